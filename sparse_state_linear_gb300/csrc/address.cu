@@ -1,0 +1,345 @@
+// address.cu -- product-key addressing on sm_103a.
+//
+// [SDM notes] "Sparse Delta Memory：中文精读笔记", 2.3: per token and head,
+// two half-score vectors of length s = sqrt(N) per branch (write, read);
+// [FwPKM notes] 2.2: those vectors as half-query x sub-key tables, and the
+// inverse-distance score -log(eps + |q - K_j|^2).
+//
+// One CTA handles one head and a tile of 16 tokens x 2 branches = 32 score
+// rows.  For each half p the 32 x s score tile is a small dense contraction
+// (32 x d_h times d_h x s) done in fp32 FFMA from shared-memory tiles and
+// kept on chip; warps then run the exact top-k of every row (select.cuh).
+// After both halves, each row's two sorted lists are merged into the best W
+// (R) slots with their softmax weights.
+#include "common.cuh"
+#include "internal.h"
+#include "select.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr int kRows = 32;       // score rows per CTA
+constexpr int kBK = 16;         // reduction chunk (d_h is a multiple of 16)
+constexpr int kBN = 256;        // sub-key chunk
+constexpr int kThreads = 256;   // 8 warps
+constexpr int kWarps = kThreads / 32;
+constexpr int kStairMax = 320;  // >= sum_{a<64} floor(64/(a+1)) = 280
+
+struct AddrArgs {
+  Dims d;
+  const void* q0;
+  const void* q1;
+  const void* K;
+  const float* f0;
+  const float* f1;
+  int32_t* idx_w;
+  float* wt_w;
+  int32_t* idx_r;
+  float* wt_r;
+  float* S;
+  unsigned* status;
+};
+
+struct SmemLayout {
+  size_t qT, kT, sc, lv, lid, ws, stair, nst, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline SmemLayout smem_layout(int s) {
+  SmemLayout L;
+  size_t o = 0;
+  L.qT = o;    o = align_up(o + sizeof(float) * kBK * kRows, 16);
+  L.kT = o;    o = align_up(o + sizeof(float) * kBK * kBN, 16);
+  L.sc = o;    o = align_up(o + sizeof(float) * kRows * (size_t)s, 16);
+  L.lv = o;    o = align_up(o + sizeof(float) * kRows * 2 * kMaxSel, 16);
+  L.lid = o;   o = align_up(o + sizeof(uint32_t) * kRows * 2 * kMaxSel, 16);
+  L.ws = o;    o = align_up(o + sizeof(WarpScratch) * kWarps, 16);
+  L.stair = o; o = align_up(o + sizeof(uint16_t) * 2 * kStairMax, 16);
+  L.nst = o;   o = align_up(o + sizeof(int) * 2, 16);
+  L.total = o;
+  return L;
+}
+
+template <int MODE>
+__device__ __forceinline__ void row_item(int r, int& sigma, long long& item) {
+  if (MODE == kAddrScoresOnly) {
+    sigma = 0;
+    item = (long long)blockIdx.x * kRows + r;
+  } else {
+    sigma = r >> 4;
+    item = (long long)blockIdx.x * (kRows / 2) + (r & 15);
+  }
+}
+
+// Score tile of half p: rows x [j0, j0+kBN) accumulated over d_h.
+template <int MODE, bool BF16, int KIND>
+__device__ void score_half(const AddrArgs& A, int p, float* qT, float* kT, float* sc) {
+  const Dims& d = A.d;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y;
+  const long long BT = (long long)d.B * d.T;
+  const int rb = 8 * (warp & 3);
+  const int cb = 128 * (warp >> 2) + 4 * lane;
+
+  // Loader roles: q tile (row = tid/8, two d-elements), K tile (row jj = tid).
+  const int lr = tid >> 3, lpart = tid & 7;
+  int lsig;
+  long long litem;
+  row_item<MODE>(lr, lsig, litem);
+  const bool lvalid = litem < BT;
+  size_t qoff = 0;
+  if (lvalid) {
+    const long long b = litem / d.T, t = litem - b * d.T;
+    const long long th = (b * d.H + h) * d.T + t;
+    qoff = (size_t)(th * 2 + p) * d.dh;
+  }
+  const void* qbase = (lsig == 0) ? A.q0 : A.q1;
+
+  for (int j0 = 0; j0 < d.s; j0 += kBN) {
+    float acc[8][4];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+
+    for (int d0 = 0; d0 < d.dh; d0 += kBK) {
+      __syncthreads();
+      // q tile: qT[dd][row]
+      {
+        float x0 = 0.f, x1 = 0.f;
+        if (lvalid) {
+          const size_t e = qoff + d0 + 2 * lpart;
+          if (BF16) {
+            const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(
+                reinterpret_cast<const __nv_bfloat16*>(qbase) + e));
+            x0 = bf16_bits_to_float(w & 0xffffu);
+            x1 = bf16_bits_to_float(w >> 16);
+          } else {
+            const float2 w = __ldg(reinterpret_cast<const float2*>(
+                reinterpret_cast<const float*>(qbase) + e));
+            x0 = w.x;
+            x1 = w.y;
+          }
+        }
+        qT[(2 * lpart) * kRows + lr] = x0;
+        qT[(2 * lpart + 1) * kRows + lr] = x1;
+      }
+      // K tile: kT[dd][jj]
+      {
+        const int j = j0 + tid;
+        float x[kBK];
+        if (j < d.s) {
+          const size_t e = ((size_t)(h * 2 + p) * d.s + j) * d.dh + d0;
+          if (BF16) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const __nv_bfloat16*>(A.K) + e);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const uint4 w = __ldg(src + u);
+              const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                x[8 * u + 2 * c] = bf16_bits_to_float(ws4[c] & 0xffffu);
+                x[8 * u + 2 * c + 1] = bf16_bits_to_float(ws4[c] >> 16);
+              }
+            }
+          } else {
+            const float4* src = reinterpret_cast<const float4*>(
+                reinterpret_cast<const float*>(A.K) + e);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float4 w = __ldg(src + u);
+              x[4 * u] = w.x;
+              x[4 * u + 1] = w.y;
+              x[4 * u + 2] = w.z;
+              x[4 * u + 3] = w.w;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBK; ++c) x[c] = 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < kBK; ++c) kT[c * kBN + tid] = x[c];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int dd = 0; dd < kBK; ++dd) {
+        const float4 qa = *reinterpret_cast<const float4*>(qT + dd * kRows + rb);
+        const float4 qb = *reinterpret_cast<const float4*>(qT + dd * kRows + rb + 4);
+        const float4 kk = *reinterpret_cast<const float4*>(kT + dd * kBN + cb);
+        const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        const float kv[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (KIND == SDM_SCORE_DOT) {
+              acc[r][c] = fmaf(qv[r], kv[c], acc[r][c]);
+            } else {
+              const float df = qv[r] - kv[c];
+              acc[r][c] = fmaf(df, df, acc[r][c]);
+            }
+          }
+      }
+    }
+    // Epilogue.
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int row = rb + r;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int col = j0 + cb + c;
+        if (col >= d.s) continue;
+        const float val = (KIND == SDM_SCORE_DOT) ? acc[r][c] : -logf(d.eps + acc[r][c]);
+        if (MODE == kAddrScoresOnly) {
+          int sg;
+          long long item;
+          row_item<MODE>(row, sg, item);
+          if (item < BT) {
+            const long long b = item / d.T, t = item - b * d.T;
+            const long long th = (b * d.H + h) * d.T + t;
+            A.S[(size_t)(th * 2 + p) * d.s + col] = val;
+          }
+        } else {
+          sc[(size_t)row * d.s + col] = val;
+        }
+      }
+    }
+  }
+}
+
+template <int MODE, bool BF16, int KIND>
+__global__ void __launch_bounds__(kThreads) address_kernel(const AddrArgs A) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const Dims& d = A.d;
+  const SmemLayout L = smem_layout(d.s);
+  float* qT = reinterpret_cast<float*>(smem + L.qT);
+  float* kT = reinterpret_cast<float*>(smem + L.kT);
+  float* sc = reinterpret_cast<float*>(smem + L.sc);
+  float* lv = reinterpret_cast<float*>(smem + L.lv);
+  uint32_t* lid = reinterpret_cast<uint32_t*>(smem + L.lid);
+  WarpScratch* wsa = reinterpret_cast<WarpScratch*>(smem + L.ws);
+  uint16_t* stair = reinterpret_cast<uint16_t*>(smem + L.stair);
+  int* nst = reinterpret_cast<int*>(smem + L.nst);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y;
+  const long long BT = (long long)d.B * d.T;
+  WarpScratch& ws = wsa[warp];
+
+  if (MODE != kAddrScoresOnly) {
+    if (warp == 0) {
+      const int n = build_stair(d.W, d.kw, stair, lane);
+      if (lane == 0) nst[0] = n;
+    } else if (warp == 1) {
+      const int n = build_stair(d.R, d.kr, stair + kStairMax, lane);
+      if (lane == 0) nst[1] = n;
+    }
+  }
+
+  for (int p = 0; p < 2; ++p) {
+    if (MODE == kAddrSelectOnly) {
+      __syncthreads();
+      for (int e = tid; e < kRows * d.s; e += kThreads) {
+        const int r = e / d.s, j = e - r * d.s;
+        int sg;
+        long long item;
+        row_item<MODE>(r, sg, item);
+        float val = 0.f;
+        if (item < BT) {
+          const long long b = item / d.T, t = item - b * d.T;
+          const long long th = (b * d.H + h) * d.T + t;
+          const float* f = sg == 0 ? A.f0 : A.f1;
+          val = __ldg(f + (size_t)(th * 2 + p) * d.s + j);
+        }
+        sc[e] = val;
+      }
+    } else {
+      score_half<MODE, BF16, KIND>(A, p, qT, kT, sc);
+    }
+    if (MODE == kAddrScoresOnly) continue;
+    __syncthreads();
+    for (int r = warp; r < kRows; r += kWarps) {
+      int sg;
+      long long item;
+      row_item<MODE>(r, sg, item);
+      if (item >= BT) continue;
+      const int k = sg == 0 ? d.kw : d.kr;
+      RowSrc src{sc + (size_t)r * d.s};
+      warp_topk_sorted(src, d.s, k, ws, lane);
+      float* ov = lv + (r * 2 + p) * kMaxSel;
+      uint32_t* oi = lid + (r * 2 + p) * kMaxSel;
+      for (int e = lane; e < k; e += 32) {
+        ov[e] = ws.out_v[e];
+        oi[e] = ws.out_id[e];
+      }
+      __syncwarp();
+    }
+  }
+  if (MODE == kAddrScoresOnly) return;
+  __syncthreads();
+  for (int r = warp; r < kRows; r += kWarps) {
+    int sg;
+    long long item;
+    row_item<MODE>(r, sg, item);
+    if (item >= BT) continue;
+    const int k = sg == 0 ? d.kw : d.kr;
+    const int nsel = sg == 0 ? d.W : d.R;
+    warp_merge(lv + (r * 2 + 0) * kMaxSel, lid + (r * 2 + 0) * kMaxSel,
+               lv + (r * 2 + 1) * kMaxSel, lid + (r * 2 + 1) * kMaxSel, k, nsel,
+               (uint32_t)d.s, stair + sg * kStairMax, nst[sg], ws, lane);
+    const long long b = item / d.T, t = item - b * d.T;
+    const long long th = (b * d.H + h) * d.T + t;
+    int32_t* io = (sg == 0 ? A.idx_w : A.idx_r) + (size_t)th * nsel;
+    float* wo = (sg == 0 ? A.wt_w : A.wt_r) + (size_t)th * nsel;
+    warp_softmax_store(ws, nsel, io, wo, lane);
+    __syncwarp();
+  }
+}
+
+template <int MODE, bool BF16, int KIND>
+cudaError_t launch_t(const AddrArgs& A, cudaStream_t stream) {
+  const SmemLayout L = smem_layout(A.d.s);
+  auto kfn = address_kernel<MODE, BF16, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)L.total);
+  if (e != cudaSuccess) return e;
+  const long long BT = (long long)A.d.B * A.d.T;
+  const int per = MODE == kAddrScoresOnly ? kRows : kRows / 2;
+  const long long tiles = (BT + per - 1) / per;
+  if (tiles == 0 || A.d.H == 0) return cudaSuccess;
+  dim3 grid((unsigned)tiles, (unsigned)A.d.H);
+  kfn<<<grid, kThreads, L.total, stream>>>(A);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_mode(const AddrArgs& A, cudaStream_t stream) {
+  const bool bf = A.d.in_dtype == SDM_BF16;
+  if (A.d.score == SDM_SCORE_DOT)
+    return bf ? launch_t<MODE, true, SDM_SCORE_DOT>(A, stream)
+              : launch_t<MODE, false, SDM_SCORE_DOT>(A, stream);
+  return bf ? launch_t<MODE, true, SDM_SCORE_IDW>(A, stream)
+            : launch_t<MODE, false, SDM_SCORE_IDW>(A, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_address(int mode, const Dims& d, const void* q0, const void* q1,
+                           const void* K, const float* f0, const float* f1,
+                           int32_t* idx_w, float* wt_w, int32_t* idx_r, float* wt_r,
+                           float* S, unsigned* status, cudaStream_t stream) {
+  AddrArgs A{d, q0, q1, K, f0, f1, idx_w, wt_w, idx_r, wt_r, S, status};
+  switch (mode) {
+    case kAddrFused: return launch_mode<kAddrFused>(A, stream);
+    case kAddrSelectOnly:
+      // Sub-scores are given: dtype and score kind do not matter.
+      return launch_t<kAddrSelectOnly, false, SDM_SCORE_DOT>(A, stream);
+    case kAddrScoresOnly: return launch_mode<kAddrScoresOnly>(A, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sdm

@@ -1,0 +1,44 @@
+// internal.h -- host-side launchers shared between the translation units of
+// the SDM library (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sdm.h"
+
+namespace sdm {
+
+// Resolved per-call parameters (validated by the API layer).
+struct Dims {
+  int B, H, T, s, dh, dv, W, R, kw, kr;
+  int in_dtype;  // SDM_F32 / SDM_BF16
+  int score;     // SDM_SCORE_DOT / SDM_SCORE_IDW
+  float eps;
+  int update;    // SDM_UPDATE_*
+#ifdef __CUDACC__
+  __host__ __device__
+#endif
+  long long N() const { return (long long)s * s; }
+};
+
+enum AddrMode { kAddrFused = 0, kAddrSelectOnly = 1, kAddrScoresOnly = 2 };
+
+// Addressing kernels (address.cu).
+//  kAddrFused:      q0 = q_w, q1 = q_r -> idx/wt of both branches.
+//  kAddrSelectOnly: f0 = sub_w, f1 = sub_r (float32 sub-scores) -> idx/wt.
+//  kAddrScoresOnly: q0 = the branch's half-queries -> S (float32).
+cudaError_t launch_address(int mode, const Dims& d, const void* q0, const void* q1,
+                           const void* K, const float* f0, const float* f1,
+                           int32_t* idx_w, float* wt_w, int32_t* idx_r, float* wt_r,
+                           float* S, unsigned* status, cudaStream_t stream);
+
+// Scan (scan.cu): the plan kernel (writes per-row source codes into
+// `workspace`) then the scan kernel.
+size_t scan_workspace_bytes(const Dims& d);
+cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
+                        const int32_t* idx_r, const float* wt_r, const void* alpha,
+                        const void* beta, const void* v, float* M, float* y, void* workspace,
+                        int depth, int col_slice, unsigned* status, cudaStream_t stream);
+
+}  // namespace sdm

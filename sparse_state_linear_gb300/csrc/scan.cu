@@ -1,0 +1,583 @@
+// scan.cu -- the sparse gated delta write and the read, sequential in t.
+//
+// [SDM notes] "Sparse Delta Memory：中文精读笔记", 2.4, Eq. (3)-(5): for each
+// selected write slot i, M~[i] = alpha_t M[i] and
+// M[i] = M~[i] + beta_t w_i (v_t - M~[i]); other rows are untouched; then
+// y_t = sum_{i in read set} q_i M_t[i] reads the table after the write.
+//
+// Parallel units: (chain = (b,h), column slice of CW floats).  The update
+// acts column by column with per-row scalars, so slices of one chain never
+// communicate, and a step's write slots are distinct, so no atomics.
+//
+// Two kernels.
+//  * plan_kernel (fully parallel over chains and blocks of steps): rows of
+//    step t are fetched while steps t-depth+1 .. t-1 may still be writing
+//    them, so for every row a step touches it records where the current
+//    value will be: -1 = the fetched copy, (d << 6) | p = the on-chip copy
+//    that step t-d left at write position p (latest such d; reads also see
+//    d = 0, the step's own write), -2 = invalid (index out of range, or a
+//    slot repeated within one write set).  One CTA hashes the write sets of
+//    a block of steps plus the depth-1 steps before it into shared memory
+//    and answers every lookup of the block in parallel.
+//  * scan_kernel, one CTA per unit: 8 consumer warps and 1 producer warp.
+//    The producer copies each step's slot lists, weights, codes and value
+//    slice into a ring of metadata slots (cp.async, several steps ahead) and
+//    turns codes into shared-memory offsets.  The consumers fetch the rows of
+//    step t+depth right after step t (cp.async, 16 B per lane, coalesced per
+//    row slice; each lane fetches exactly the chunks it later uses), so depth
+//    steps of row traffic are in flight per unit.  A step is: wait for own
+//    chunks, decay + delta on the write rows (kept on chip, stored to HBM),
+//    ONE block barrier, weighted read, warp reduction into a per-warp
+//    partial; one warp sums the partials of step t after the next barrier.
+//  Every wait is bounded (seconds); a wait that runs out records
+//  SDM_ERR_TIMEOUT in the status word and the CTA leaves cleanly.
+#include "common.cuh"
+#include "internal.h"
+
+namespace sdm {
+namespace {
+
+constexpr int kConsumers = 256;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kP = 4;            // producer's metadata prefetch distance (steps)
+constexpr int kSlack = 4;        // steps the producer may prepare beyond the need
+constexpr uint32_t kFwd = 1u << 30;   // src flag: forwarded, do not fetch
+constexpr uint32_t kSkip = 1u << 31;  // src flag: invalid row, ignore
+constexpr uint32_t kOffMask = 0x00ffffffu;
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+
+// Plan kernel.
+constexpr int kPlanTB = 64;          // steps per plan CTA
+constexpr int kPlanThreads = 256;
+constexpr int kPlanHash = 16384;     // hash entries (uint32) in shared memory
+constexpr uint32_t kPlanEmpty = 0xffffffffu;
+
+struct MetaSlot {
+  int32_t idx_w[64];
+  int32_t idx_r[64];
+  float wt_w[64];
+  float wt_r[64];
+  uint32_t src_w[64];     // shared-memory byte offset of the row's chunk 0 | flags
+  uint32_t src_r[64];
+  int16_t code[128];      // plan codes: W write rows then R read rows
+  unsigned char vraw[128];
+  float alpha, beta, pad0, pad1;
+  unsigned char pad[112];
+};
+static_assert(sizeof(MetaSlot) == 2048, "meta slot size");
+
+struct ScanArgs {
+  Dims d;
+  const int32_t* idx_w;
+  const float* wt_w;
+  const int32_t* idx_r;
+  const float* wt_r;
+  const void* alpha;
+  const void* beta;
+  const void* v;
+  const int16_t* codes;
+  float* M;
+  float* y;
+  int depth;
+  unsigned* status;
+};
+
+struct ScanLayout {
+  size_t meta, wtile, rtile, ypart, bars, total;
+  int NS, MR;
+};
+
+__host__ __device__ inline ScanLayout scan_layout(int CW, int W, int R, int D) {
+  ScanLayout L;
+  L.NS = 2 * D;
+  L.MR = D + kP + 1 + kSlack;
+  size_t o = 0;
+  L.meta = o;  o += sizeof(MetaSlot) * L.MR;
+  L.wtile = o; o += sizeof(float) * (size_t)L.NS * W * CW;
+  L.rtile = o; o += sizeof(float) * (size_t)D * R * CW;
+  L.ypart = o; o += sizeof(float) * 2 * 8 * CW;
+  L.bars = o;  o += sizeof(uint64_t) * 2 * L.MR;
+  L.total = o;
+  return L;
+}
+
+// Codes per token: W + R rounded up to 8 (16-byte rows).
+__host__ __device__ inline int code_pitch(int W, int R) { return (W + R + 7) & ~7; }
+
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    case 7: cp_async_wait<7>(); break;
+    case 8: cp_async_wait<8>(); break;
+    case 9: cp_async_wait<9>(); break;
+    case 10: cp_async_wait<10>(); break;
+    case 11: cp_async_wait<11>(); break;
+    case 12: cp_async_wait<12>(); break;
+    case 13: cp_async_wait<13>(); break;
+    case 14: cp_async_wait<14>(); break;
+    default: cp_async_wait<15>(); break;
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float4 load_v4(const unsigned char* vraw, int c) {
+  if (BF16) {
+    const uint2 w = *reinterpret_cast<const uint2*>(vraw + 8 * c);
+    return make_float4(bf16_bits_to_float(w.x & 0xffffu), bf16_bits_to_float(w.x >> 16),
+                       bf16_bits_to_float(w.y & 0xffffu), bf16_bits_to_float(w.y >> 16));
+  }
+  return *reinterpret_cast<const float4*>(vraw + 16 * c);
+}
+
+// ------------------------------------------------------------------ plan
+struct PlanArgs {
+  const int32_t* idx_w;
+  const int32_t* idx_r;
+  int16_t* codes;
+  int T, W, R, depth;
+  uint32_t N;
+  unsigned* status;
+};
+
+__device__ __forceinline__ uint32_t plan_hash(uint32_t row) {
+  return (row * 0x9E3779B1u) >> (32 - 14);
+}
+
+// Entry = (row << 13) | (step - s0) << 6 | position; rows < 2^18, step offsets
+// < 128 (kPlanTB + depth - 1), positions < 64.
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs P) {
+  extern __shared__ __align__(16) uint32_t tab[];
+  const int chain = blockIdx.y;
+  const int t0 = blockIdx.x * kPlanTB;
+  const int t1 = min(P.T, t0 + kPlanTB);
+  const int s0 = max(0, t0 - (P.depth - 1));
+  const int W = P.W, R = P.R, WR = W + R, CP = code_pitch(W, R);
+  const size_t base = (size_t)chain * P.T;
+  for (int i = threadIdx.x; i < kPlanHash / 4; i += kPlanThreads)
+    reinterpret_cast<uint4*>(tab)[i] = make_uint4(kPlanEmpty, kPlanEmpty, kPlanEmpty, kPlanEmpty);
+  __syncthreads();
+  const int nins = (t1 - s0) * W;
+  for (int e = threadIdx.x; e < nins; e += kPlanThreads) {
+    const int ds = e / W, j = e - ds * W;
+    const int row = __ldg(P.idx_w + (base + s0 + ds) * W + j);
+    if (row < 0 || (uint32_t)row >= P.N) continue;
+    const uint32_t key = ((uint32_t)row << 13) | ((uint32_t)ds << 6) | (uint32_t)j;
+    uint32_t h = plan_hash((uint32_t)row);
+    for (int i = 0; i < kPlanHash; ++i) {
+      if (atomicCAS(&tab[h], kPlanEmpty, key) == kPlanEmpty) break;
+      h = (h + 1) & (kPlanHash - 1);
+    }
+  }
+  __syncthreads();
+  const int nlook = (t1 - t0) * WR;
+  for (int e = threadIdx.x; e < nlook; e += kPlanThreads) {
+    const int dt = e / WR, k = e - dt * WR;
+    const int t = t0 + dt;
+    const bool is_w = k < W;
+    const int row = is_w ? __ldg(P.idx_w + (base + t) * W + k)
+                         : __ldg(P.idx_r + (base + t) * R + (k - W));
+    int code = -1;
+    if (row < 0 || (uint32_t)row >= P.N) {
+      record_status(P.status, SDM_ERR_DEVICE_BOUNDS);
+      code = -2;
+    } else {
+      // Latest writer s of this row with t-depth+1 <= s < t (<= t for reads).
+      const int lo = t - (P.depth - 1), hi = is_w ? t - 1 : t;
+      int best = -1, bp = 0;
+      bool dup = false;
+      uint32_t h = plan_hash((uint32_t)row);
+      for (int i = 0; i < kPlanHash; ++i) {
+        const uint32_t ent = tab[h];
+        if (ent == kPlanEmpty) break;
+        if ((ent >> 13) == (uint32_t)row) {
+          const int s = s0 + (int)((ent >> 6) & 127u), p = (int)(ent & 63u);
+          if (is_w && s == t && p != k) dup = true;
+          if (s >= lo && s <= hi && s > best) {
+            best = s;
+            bp = p;
+          }
+        }
+        h = (h + 1) & (kPlanHash - 1);
+      }
+      if (dup) {
+        record_status(P.status, SDM_ERR_DUPLICATE_SLOT);
+        code = -2;
+      } else if (best >= 0) {
+        code = ((t - best) << 6) | bp;
+      }
+    }
+    P.codes[(base + t) * CP + k] = (int16_t)code;
+  }
+}
+
+// Ring position that advances by one step at a time (no division).
+struct Ring {
+  int i, n;
+  unsigned phase;
+  __device__ __forceinline__ void next() {
+    if (++i == n) {
+      i = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+template <int CW, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1) scan_kernel(const ScanArgs A) {
+  constexpr int CH = CW / 4;               // 16-byte chunks per row slice
+  constexpr int RP = kConsumers / CH;      // rows per consumer pass
+  constexpr int IB = BF16 ? 2 : 4;         // input element bytes
+  extern __shared__ __align__(16) unsigned char smem[];
+
+  const Dims& d = A.d;
+  const int D = A.depth;
+  const int W = d.W, R = d.R, T = d.T, dv = d.dv;
+  const ScanLayout L = scan_layout(CW, W, R, D);
+  const int NS = L.NS, MR = L.MR;
+  const int nslice = dv / CW;
+  const int chain = blockIdx.x / nslice;
+  const int c0 = (blockIdx.x - chain * nslice) * CW;
+  const size_t th0 = (size_t)chain * T;    // flat (b,h,t=0) row
+  float* Mc = A.M + (size_t)chain * (size_t)d.N() * dv + c0;
+  const int CP = code_pitch(W, R);
+
+  MetaSlot* meta = reinterpret_cast<MetaSlot*>(smem + L.meta);
+  float* ypart = reinterpret_cast<float*>(smem + L.ypart);
+  uint64_t* mfull = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* mempty = mfull + MR;
+  const uint32_t wslot = (uint32_t)(W * CW * 4), rslot = (uint32_t)(R * CW * 4);
+  constexpr uint32_t rowb = (uint32_t)(CW * 4);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int i = 0; i < MR; ++i) {
+      mbar_init(&mfull[i], 32);
+      mbar_init(&mempty[i], kConsumers / 32);
+    }
+  }
+  __syncthreads();
+
+  if (warp == kConsumers / 32) {
+    // ------------------------------------------------------------ producer
+    float ga_cur = 0.f, gb_cur = 0.f, ga_nxt = 0.f, gb_nxt = 0.f;
+    if (lane < T) {
+      ga_cur = load_scalar(A.alpha, th0 + lane, d.in_dtype);
+      gb_cur = load_scalar(A.beta, th0 + lane, d.in_dtype);
+    }
+    if (32 + lane < T) {
+      ga_nxt = load_scalar(A.alpha, th0 + 32 + lane, d.in_dtype);
+      gb_nxt = load_scalar(A.beta, th0 + 32 + lane, d.in_dtype);
+    }
+    const bool vec_w = (W & 3) == 0, vec_r = (R & 3) == 0;
+    Ring mi{0, MR, 0u};         // slot of step u (copy stage)
+    Ring mp{0, MR, 0u};         // slot of step up = u - kP (decode stage)
+    Ring wp{0, NS, 0u};         // write-tile slot of step up
+    Ring rp{0, D, 0u};          // read-tile slot of step up
+    for (int u = 0; u < T + kP; ++u) {
+      if (u < T) {
+        if (u >= MR) {
+          // Slot reuse: step u - MR must be finished by the consumers.
+          bool ok = mbar_try_wait(&mempty[mi.i], mi.phase ^ 1u);
+          if (!ok) {
+            const uint64_t t0 = global_ns();
+            while (!(ok = mbar_try_wait(&mempty[mi.i], mi.phase ^ 1u))) {
+              __nanosleep(64);
+              if (global_ns() - t0 > kTimeoutNs) break;
+            }
+          }
+          if (!ok) {
+            record_status(A.status, SDM_ERR_TIMEOUT);
+            break;
+          }
+        }
+        MetaSlot* m = meta + mi.i;
+        const size_t th = th0 + u;
+        if (vec_w) {
+          for (int c = lane; c < W / 4; c += 32) {
+            cp_async16(&m->idx_w[4 * c], A.idx_w + th * W + 4 * c);
+            cp_async16(&m->wt_w[4 * c], A.wt_w + th * W + 4 * c);
+          }
+        } else {
+          for (int j = lane; j < W; j += 32) {
+            cp_async4(&m->idx_w[j], A.idx_w + th * W + j);
+            cp_async4(&m->wt_w[j], A.wt_w + th * W + j);
+          }
+        }
+        if (vec_r) {
+          for (int c = lane; c < R / 4; c += 32) {
+            cp_async16(&m->idx_r[4 * c], A.idx_r + th * R + 4 * c);
+            cp_async16(&m->wt_r[4 * c], A.wt_r + th * R + 4 * c);
+          }
+        } else {
+          for (int j = lane; j < R; j += 32) {
+            cp_async4(&m->idx_r[j], A.idx_r + th * R + j);
+            cp_async4(&m->wt_r[j], A.wt_r + th * R + j);
+          }
+        }
+        if (lane < CP / 8) cp_async16(&m->code[8 * lane], A.codes + th * CP + 8 * lane);
+        if (lane < CW * IB / 16)
+          cp_async16(m->vraw + 16 * lane,
+                     reinterpret_cast<const unsigned char*>(A.v) + (th * dv + c0) * IB + 16 * lane);
+        mi.next();
+      }
+      cp_async_commit();
+      if (u < kP) continue;
+
+      // ---- step up: gates, and the shared-memory source of every row.
+      const int up = u - kP;
+      cp_async_wait<kP>();
+      __syncwarp();
+      MetaSlot* m = meta + mp.i;
+      if ((up & 31) == 0 && up > 0) {
+        ga_cur = ga_nxt;
+        gb_cur = gb_nxt;
+        if (up + 32 + lane < T) {
+          ga_nxt = load_scalar(A.alpha, th0 + up + 32 + lane, d.in_dtype);
+          gb_nxt = load_scalar(A.beta, th0 + up + 32 + lane, d.in_dtype);
+        }
+      }
+      const float ga = __shfl_sync(0xffffffffu, ga_cur, up & 31);
+      const float gb = __shfl_sync(0xffffffffu, gb_cur, up & 31);
+      if (lane == 0) {
+        m->alpha = ga;
+        m->beta = gb;
+      }
+      const int wcur = wp.i;
+      const uint32_t wbase = (uint32_t)L.wtile, rbase = (uint32_t)L.rtile + rp.i * rslot;
+      for (int k = lane; k < W + R; k += 32) {
+        const int c = m->code[k];
+        uint32_t src;
+        if (c == -2) {
+          src = kSkip;
+        } else if (c >= 0) {
+          const int dd = c >> 6, p = c & 63;
+          const int sl = wcur >= dd ? wcur - dd : wcur - dd + NS;
+          src = (wbase + sl * wslot + p * rowb) | kFwd;
+        } else if (k < W) {
+          src = wbase + wcur * wslot + k * rowb;
+        } else {
+          src = rbase + (k - W) * rowb;
+        }
+        if (k < W) m->src_w[k] = src; else m->src_r[k - W] = src;
+      }
+      __syncwarp();
+      mbar_arrive(&mfull[mp.i]);
+      mp.next();
+      wp.next();
+      rp.next();
+    }
+    cp_async_wait_all();
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int myc = tid % CH, myr = tid / CH;
+  const int PW = (W + RP - 1) / RP, PR = (R + RP - 1) / RP;
+  float* Mt = Mc + 4 * myc;                  // this lane's column chunk of row 0
+  unsigned char* sm_c = smem + 16 * myc;     // shared base shifted to the chunk
+  bool aborted = false;
+
+  auto wait_meta = [&](const Ring& r) {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(&mfull[r.i], r.phase, kTimeoutNs);
+    __syncwarp();
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);
+      aborted = true;
+    }
+  };
+  auto issue = [&](const MetaSlot* m) {
+    for (int pw = 0; pw < PW; ++pw) {
+      const int j = pw * RP + myr;
+      if (j >= W) break;
+      const uint32_t s = m->src_w[j];
+      const int row = m->idx_w[j];
+      if (!(s & (kFwd | kSkip))) cp_async16(sm_c + (s & kOffMask), Mt + (size_t)row * dv);
+    }
+    for (int pr = 0; pr < PR; ++pr) {
+      const int q = pr * RP + myr;
+      if (q >= R) break;
+      const uint32_t s = m->src_r[q];
+      const int row = m->idx_r[q];
+      if (!(s & (kFwd | kSkip))) cp_async16(sm_c + (s & kOffMask), Mt + (size_t)row * dv);
+    }
+  };
+  auto finalize = [&](int t) {
+    if (lane < CH) {
+      const float* yp = ypart + (t & 1) * 8 * CW + 4 * lane;
+      float4 s4 = *reinterpret_cast<const float4*>(yp);
+#pragma unroll
+      for (int w = 1; w < 8; ++w) {
+        const float4 p = *reinterpret_cast<const float4*>(yp + w * CW);
+        s4.x += p.x;
+        s4.y += p.y;
+        s4.z += p.z;
+        s4.w += p.w;
+      }
+      *reinterpret_cast<float4*>(A.y + (th0 + t) * dv + c0 + 4 * lane) = s4;
+    }
+  };
+
+  Ring mt{0, MR, 0u};   // metadata slot of step t
+  Ring mu{0, MR, 0u};   // metadata slot of step t + D (next to fetch)
+  Ring wt{0, NS, 0u};   // write-tile slot of step t
+  for (int u = 0; u < D; ++u) {
+    if (u < T && !aborted) {
+      wait_meta(mu);
+      if (!aborted) issue(meta + mu.i);
+    }
+    if (u < T) mu.next();
+    cp_async_commit();
+  }
+
+  for (int t = 0; t < T; ++t) {
+    cp_async_wait_dyn(D - 1);
+    const MetaSlot* m = meta + mt.i;
+    if (!aborted) {
+      // Write: decay + per-slot delta (Eq. (3)-(4)).
+      const float a = m->alpha, b = m->beta;
+      const float4 vv = load_v4<BF16>(m->vraw, myc);
+      unsigned char* wdst = sm_c + L.wtile + wt.i * wslot;
+      for (int pw = 0; pw < PW; ++pw) {
+        const int j = pw * RP + myr;
+        if (j >= W) break;
+        const uint32_t s = m->src_w[j];
+        const int row = m->idx_w[j];
+        const float wj = m->wt_w[j];
+        float4 x = *reinterpret_cast<const float4*>(wdst + j * rowb);   // fetched copy
+        if (s & (kFwd | kSkip)) {
+          if (s & kSkip) continue;
+          x = *reinterpret_cast<const float4*>(sm_c + (s & kOffMask));  // forwarded copy
+        }
+        const float cw = b * wj;
+        float4 o;
+        float mt_;
+        mt_ = a * x.x; o.x = fmaf(cw, vv.x - mt_, mt_);
+        mt_ = a * x.y; o.y = fmaf(cw, vv.y - mt_, mt_);
+        mt_ = a * x.z; o.z = fmaf(cw, vv.z - mt_, mt_);
+        mt_ = a * x.w; o.w = fmaf(cw, vv.w - mt_, mt_);
+        *reinterpret_cast<float4*>(wdst + j * rowb) = o;
+        *reinterpret_cast<float4*>(Mt + (size_t)row * dv) = o;
+      }
+    }
+    // The one block barrier of a step; it also turns a timeout anywhere
+    // into a decision every consumer takes at the same point.
+    if (named_bar_or(1, kConsumers, aborted)) {
+      aborted = true;
+      break;
+    }
+    if (t > 0 && warp == ((t - 1) & 7)) finalize(t - 1);
+
+    // Read after the write (Eq. (5)).
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int pr = 0; pr < PR; ++pr) {
+      const int q = pr * RP + myr;
+      if (q >= R) break;
+      const uint32_t s = m->src_r[q];
+      const float w = m->wt_r[q];
+      if (s & kSkip) continue;
+      const float4 x = *reinterpret_cast<const float4*>(sm_c + (s & kOffMask));
+      acc.x = fmaf(w, x.x, acc.x);
+      acc.y = fmaf(w, x.y, acc.y);
+      acc.z = fmaf(w, x.z, acc.z);
+      acc.w = fmaf(w, x.w, acc.w);
+    }
+#pragma unroll
+    for (int off = CH; off < 32; off <<= 1) {
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+    }
+    if (lane < CH) *reinterpret_cast<float4*>(ypart + (t & 1) * 8 * CW + warp * CW + 4 * lane) = acc;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&mempty[mt.i]);
+    if (t + D < T) {
+      if (!aborted) {
+        wait_meta(mu);
+        if (!aborted) issue(meta + mu.i);
+      }
+      mu.next();
+    }
+    cp_async_commit();
+    mt.next();
+    wt.next();
+  }
+  named_bar_sync(1, kConsumers);
+  if (!aborted && T > 0 && warp == ((T - 1) & 7)) finalize(T - 1);
+  cp_async_wait_all();
+}
+
+template <int CW, bool BF16>
+cudaError_t launch_t(const ScanArgs& A, cudaStream_t stream) {
+  const size_t smem = scan_layout(CW, A.d.W, A.d.R, A.depth).total;
+  auto kfn = scan_kernel<CW, BF16>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long units = (long long)A.d.B * A.d.H * (A.d.dv / CW);
+  if (units == 0 || A.d.T == 0) return cudaSuccess;
+  kfn<<<(unsigned)units, kThreads, smem, stream>>>(A);
+  return cudaGetLastError();
+}
+
+constexpr size_t kSmemPerSM = 233472;   // 228 KiB
+constexpr size_t kSmemMaxCTA = 232448;  // 227 KiB
+constexpr int kSMs = 152;
+
+}  // namespace
+
+size_t scan_workspace_bytes(const Dims& d) {
+  return (size_t)d.B * d.H * d.T * code_pitch(d.W, d.R) * sizeof(int16_t);
+}
+
+cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
+                        const int32_t* idx_r, const float* wt_r, const void* alpha,
+                        const void* beta, const void* v, float* M, float* y, void* workspace,
+                        int depth, int col_slice, unsigned* status, cudaStream_t stream) {
+  const long long chains = (long long)d.B * d.H;
+  if (chains == 0 || d.T == 0) return cudaSuccess;
+  int cw = col_slice;
+  if (cw == 0) cw = (d.dv % 32 == 0 && chains * (d.dv / 32) >= kSMs) ? 32 : 16;
+  if (d.dv % cw != 0) cw = 16;
+  const long long units = chains * (d.dv / cw);
+  // CTAs per SM needed to keep every unit resident, and the ring depth that fits.
+  const long long per_sm = (units + kSMs - 1) / kSMs;
+  const size_t budget =
+      per_sm <= 1 ? kSmemMaxCTA : (per_sm == 2 ? kSmemPerSM / 2 - 1024 : kSmemPerSM / 3 - 1024);
+  int D = depth;
+  if (D == 0) {
+    D = 1;
+    for (int cand = 2; cand <= 16; ++cand)
+      if (scan_layout(cw, d.W, d.R, cand).total <= budget) D = cand;
+  }
+  if (D < 1 || D > 16) return cudaErrorInvalidValue;
+  // A requested depth is a hint: shrink it until the ring fits on chip.
+  while (D > 1 && scan_layout(cw, d.W, d.R, D).total > kSmemMaxCTA) --D;
+
+  int16_t* codes = static_cast<int16_t*>(workspace);
+  {
+    const size_t smem = sizeof(uint32_t) * kPlanHash;
+    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    PlanArgs P{idx_w, idx_r, codes, d.T, d.W, d.R, D, (uint32_t)d.N(), status};
+    dim3 grid((unsigned)((d.T + kPlanTB - 1) / kPlanTB), (unsigned)chains);
+    plan_kernel<<<grid, kPlanThreads, smem, stream>>>(P);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  ScanArgs A{d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, codes, M, y, D, status};
+  const bool bf = d.in_dtype == SDM_BF16;
+  if (cw == 32) return bf ? launch_t<32, true>(A, stream) : launch_t<32, false>(A, stream);
+  return bf ? launch_t<16, true>(A, stream) : launch_t<16, false>(A, stream);
+}
+
+}  // namespace sdm

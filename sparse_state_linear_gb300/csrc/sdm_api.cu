@@ -1,0 +1,271 @@
+// sdm_api.cu -- the C ABI declared in include/sdm.h: argument checks, the
+// per-device status word, and kernel dispatch.  No device memory is
+// allocated here; every tensor belongs to the caller.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sdm.h"
+
+namespace sdm {
+namespace {
+
+// The status word of each device that loads this library (see sdm.h).
+__device__ unsigned g_status = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_status_ptr[kMaxDevices] = {};
+int g_depth = 0, g_colslice = 0;
+
+sdm_status status_ptr(unsigned** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return SDM_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return SDM_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return SDM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sdm_status check_shape(const sdm_shape* sh, Dims* d) {
+  if (!sh) return SDM_ERR_INVALID_ARG;
+  if (sh->B < 0 || sh->H < 0 || sh->T < 0) return SDM_ERR_INVALID_ARG;
+  if (sh->n_sub < 1 || sh->d_h < 1 || sh->d_v < 1 || sh->W < 1 || sh->R < 1)
+    return SDM_ERR_INVALID_ARG;
+  if (sh->k_w < 0 || sh->k_r < 0) return SDM_ERR_INVALID_ARG;
+  if (sh->in_dtype != SDM_F32 && sh->in_dtype != SDM_BF16) return SDM_ERR_INVALID_ARG;
+  if (sh->score != SDM_SCORE_DOT && sh->score != SDM_SCORE_IDW) return SDM_ERR_INVALID_ARG;
+  if (sh->update != SDM_UPDATE_EQ4 && sh->update != SDM_UPDATE_SHARED_RESIDUAL)
+    return SDM_ERR_INVALID_ARG;
+  if (sh->score == SDM_SCORE_IDW && !(sh->idw_eps > 0.f)) return SDM_ERR_INVALID_ARG;
+  const int s = sh->n_sub;
+  const int kw = sh->k_w ? sh->k_w : (sh->W < s ? sh->W : s);
+  const int kr = sh->k_r ? sh->k_r : (sh->R < s ? sh->R : s);
+  if (kw > s || kr > s) return SDM_ERR_INVALID_ARG;
+  if ((long long)kw * kw < sh->W || (long long)kr * kr < sh->R) return SDM_ERR_INVALID_ARG;
+  // Supported envelope.
+  if (s > 512) return SDM_ERR_UNSUPPORTED;
+  if (sh->d_h != 16 && sh->d_h != 32 && sh->d_h != 64 && sh->d_h != 128 && sh->d_h != 256)
+    return SDM_ERR_UNSUPPORTED;
+  if (sh->d_v % 16 != 0 || sh->d_v > 1024) return SDM_ERR_UNSUPPORTED;
+  if (sh->W > 64 || sh->R > 64 || kw > 64 || kr > 64) return SDM_ERR_UNSUPPORTED;
+  if (sh->update != SDM_UPDATE_EQ4) return SDM_ERR_UNSUPPORTED;
+  const long long N = (long long)s * s;
+  if ((long long)sh->B * sh->H * N * sh->d_v >= (1ll << 40)) return SDM_ERR_UNSUPPORTED;
+  if ((long long)sh->B * sh->H * sh->T >= (1ll << 31)) return SDM_ERR_UNSUPPORTED;
+  if ((long long)sh->B * sh->T >= (1ll << 31) / 16) return SDM_ERR_UNSUPPORTED;
+  d->B = sh->B;
+  d->H = sh->H;
+  d->T = sh->T;
+  d->s = s;
+  d->dh = sh->d_h;
+  d->dv = sh->d_v;
+  d->W = sh->W;
+  d->R = sh->R;
+  d->kw = kw;
+  d->kr = kr;
+  d->in_dtype = sh->in_dtype;
+  d->score = sh->score;
+  d->eps = sh->idw_eps;
+  d->update = sh->update;
+  return SDM_OK;
+}
+
+bool empty_work(const Dims& d) { return (long long)d.B * d.H * d.T == 0; }
+
+sdm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SDM_OK : SDM_ERR_CUDA; }
+
+#define SDM_CHECK_PTR(p) \
+  do {                   \
+    if (!(p) || !aligned16(p)) return SDM_ERR_INVALID_ARG; \
+  } while (0)
+
+__global__ void wait_timeout_selftest(unsigned* status, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) mbar_init(&bar, 1);
+  __syncthreads();
+  // Nothing arrives on `bar`: the bounded wait must give up and report.
+  if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0, timeout_ns))
+    record_status(status, SDM_ERR_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace sdm
+
+using namespace sdm;
+
+extern "C" {
+
+const char* sdm_status_string(sdm_status st) {
+  switch (st) {
+    case SDM_OK: return "ok";
+    case SDM_ERR_INVALID_ARG: return "invalid argument";
+    case SDM_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case SDM_ERR_CUDA: return "CUDA runtime error";
+    case SDM_ERR_TIMEOUT: return "device wait timed out";
+    case SDM_ERR_DEVICE_BOUNDS: return "slot index out of range";
+    case SDM_ERR_DUPLICATE_SLOT: return "duplicate slot in a write set";
+  }
+  return "unknown status";
+}
+
+sdm_status sdm_subscores(const sdm_shape* shape, const void* q, const void* K, float* S,
+                         void* stream) {
+  Dims d;
+  sdm_status st = check_shape(shape, &d);
+  if (st != SDM_OK) return st;
+  SDM_CHECK_PTR(q);
+  SDM_CHECK_PTR(K);
+  SDM_CHECK_PTR(S);
+  if (empty_work(d)) return SDM_OK;
+  unsigned* sp = nullptr;
+  if ((st = status_ptr(&sp)) != SDM_OK) return st;
+  return from_cuda(launch_address(kAddrScoresOnly, d, q, nullptr, K, nullptr, nullptr,
+                                  nullptr, nullptr, nullptr, nullptr, S, sp,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+sdm_status sdm_select(const sdm_shape* shape, const float* sub_w, const float* sub_r,
+                      int32_t* idx_w, float* wt_w, int32_t* idx_r, float* wt_r,
+                      void* stream) {
+  Dims d;
+  sdm_status st = check_shape(shape, &d);
+  if (st != SDM_OK) return st;
+  SDM_CHECK_PTR(sub_w);
+  SDM_CHECK_PTR(sub_r);
+  SDM_CHECK_PTR(idx_w);
+  SDM_CHECK_PTR(wt_w);
+  SDM_CHECK_PTR(idx_r);
+  SDM_CHECK_PTR(wt_r);
+  if (empty_work(d)) return SDM_OK;
+  unsigned* sp = nullptr;
+  if ((st = status_ptr(&sp)) != SDM_OK) return st;
+  return from_cuda(launch_address(kAddrSelectOnly, d, nullptr, nullptr, nullptr, sub_w,
+                                  sub_r, idx_w, wt_w, idx_r, wt_r, nullptr, sp,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+sdm_status sdm_address(const sdm_shape* shape, const void* q_w, const void* q_r,
+                       const void* K, int32_t* idx_w, float* wt_w, int32_t* idx_r,
+                       float* wt_r, void* stream) {
+  Dims d;
+  sdm_status st = check_shape(shape, &d);
+  if (st != SDM_OK) return st;
+  SDM_CHECK_PTR(q_w);
+  SDM_CHECK_PTR(q_r);
+  SDM_CHECK_PTR(K);
+  SDM_CHECK_PTR(idx_w);
+  SDM_CHECK_PTR(wt_w);
+  SDM_CHECK_PTR(idx_r);
+  SDM_CHECK_PTR(wt_r);
+  if (empty_work(d)) return SDM_OK;
+  unsigned* sp = nullptr;
+  if ((st = status_ptr(&sp)) != SDM_OK) return st;
+  return from_cuda(launch_address(kAddrFused, d, q_w, q_r, K, nullptr, nullptr, idx_w, wt_w,
+                                  idx_r, wt_r, nullptr, sp, static_cast<cudaStream_t>(stream)));
+}
+
+size_t sdm_workspace_size(const sdm_shape* shape) {
+  Dims d;
+  if (check_shape(shape, &d) != SDM_OK) return 0;
+  return scan_workspace_bytes(d);
+}
+
+sdm_status sdm_scan(const sdm_shape* shape, const int32_t* idx_w, const float* wt_w,
+                    const int32_t* idx_r, const float* wt_r, const void* alpha,
+                    const void* beta, const void* v, float* M, float* y, void* workspace,
+                    size_t ws_bytes, void* stream) {
+  Dims d;
+  sdm_status st = check_shape(shape, &d);
+  if (st != SDM_OK) return st;
+  SDM_CHECK_PTR(idx_w);
+  SDM_CHECK_PTR(wt_w);
+  SDM_CHECK_PTR(idx_r);
+  SDM_CHECK_PTR(wt_r);
+  SDM_CHECK_PTR(alpha);
+  SDM_CHECK_PTR(beta);
+  SDM_CHECK_PTR(v);
+  SDM_CHECK_PTR(M);
+  SDM_CHECK_PTR(y);
+  if (empty_work(d)) return SDM_OK;
+  SDM_CHECK_PTR(workspace);
+  if (ws_bytes < scan_workspace_bytes(d)) return SDM_ERR_INVALID_ARG;
+  unsigned* sp = nullptr;
+  if ((st = status_ptr(&sp)) != SDM_OK) return st;
+  int depth, cs;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    depth = g_depth;
+    cs = g_colslice;
+  }
+  if (cs && d.dv % cs != 0) return SDM_ERR_INVALID_ARG;
+  return from_cuda(launch_scan(d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, workspace,
+                               depth, cs, sp, static_cast<cudaStream_t>(stream)));
+}
+
+sdm_status sdm_forward(const sdm_shape* shape, const void* q_w, const void* q_r,
+                       const void* K, const void* alpha, const void* beta, const void* v,
+                       float* M, float* y, int32_t* idx_w, float* wt_w, int32_t* idx_r,
+                       float* wt_r, void* workspace, size_t ws_bytes, void* stream) {
+  // Check the scan's arguments too before anything is enqueued.
+  Dims d;
+  sdm_status st = check_shape(shape, &d);
+  if (st != SDM_OK) return st;
+  SDM_CHECK_PTR(alpha);
+  SDM_CHECK_PTR(beta);
+  SDM_CHECK_PTR(v);
+  SDM_CHECK_PTR(M);
+  SDM_CHECK_PTR(y);
+  if (!empty_work(d)) {
+    SDM_CHECK_PTR(workspace);
+    if (ws_bytes < scan_workspace_bytes(d)) return SDM_ERR_INVALID_ARG;
+  }
+  st = sdm_address(shape, q_w, q_r, K, idx_w, wt_w, idx_r, wt_r, stream);
+  if (st != SDM_OK) return st;
+  return sdm_scan(shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, workspace, ws_bytes,
+                  stream);
+}
+
+sdm_status sdm_get_device_status(void* stream) {
+  unsigned* sp = nullptr;
+  sdm_status st = status_ptr(&sp);
+  if (st != SDM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SDM_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, sp, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SDM_ERR_CUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpy(sp, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return SDM_ERR_CUDA;
+  return static_cast<sdm_status>(v);
+}
+
+sdm_status sdm_set_scan_tuning(int depth, int col_slice) {
+  if (depth < 0 || depth > 16) return SDM_ERR_INVALID_ARG;
+  if (col_slice != 0 && col_slice != 16 && col_slice != 32) return SDM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_depth = depth;
+  g_colslice = col_slice;
+  return SDM_OK;
+}
+
+sdm_status sdm_selftest_wait_timeout(long long timeout_ns, void* stream) {
+  if (timeout_ns < 1000000ll || timeout_ns > 10000000000ll) return SDM_ERR_INVALID_ARG;
+  unsigned* sp = nullptr;
+  sdm_status st = status_ptr(&sp);
+  if (st != SDM_OK) return st;
+  wait_timeout_selftest<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      sp, (unsigned long long)timeout_ns);
+  return from_cuda(cudaGetLastError());
+}
+
+}  // extern "C"

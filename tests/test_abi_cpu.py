@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/sdm.h declares, and rejects bad arguments before it
+touches CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_state_linear_gb300 as sdm
+from sparse_state_linear_gb300 import build_ext
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_ext.build()
+    return sdm.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "sdm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdm_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(sdm.EXPORTS)
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert sdm.status_string(code) not in ("", "unknown status")
+    assert sdm.status_string(99) == "unknown status"
+
+
+def good_shape(**kw):
+    base = dict(B=2, H=2, T=8, n_sub=16, d_h=16, d_v=32, W=8, R=8, in_dtype=sdm.SDM_F32)
+    base.update(kw)
+    return sdm.make_shape(**base)
+
+
+FAKE = ctypes.c_void_p(1 << 20)        # aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p((1 << 20) + 4)
+
+
+def scan_rc(L, sh, ptrs=None, ws_bytes=1 << 30):
+    p = ptrs or [FAKE] * 9
+    return L.sdm_scan(ctypes.byref(sh), *p, FAKE, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), 1), (dict(n_sub=0), 1), (dict(W=0), 1), (dict(d_v=0), 1),
+    (dict(in_dtype=7), 1), (dict(score=3), 1), (dict(update=5), 1),
+    (dict(W=300), 1),                    # W > k_w^2 with k_w = min(W, s) = 16
+    (dict(k_w=17), 1),                   # k above s
+    (dict(n_sub=600), 2), (dict(d_h=24), 2), (dict(d_v=40), 2), (dict(n_sub=32, W=65, R=8), 2),
+    (dict(update=1), 2),
+])
+def test_scan_rejects_bad_shapes(L, kw, code):
+    assert scan_rc(L, good_shape(**kw)) == code
+
+
+def test_null_and_misaligned_pointers(L):
+    sh = good_shape()
+    for i in range(9):
+        p = [FAKE] * 9
+        p[i] = None
+        assert scan_rc(L, sh, p) == 1
+        p[i] = MISALIGNED
+        assert scan_rc(L, sh, p) == 1
+    assert L.sdm_address(ctypes.byref(sh), None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert L.sdm_select(ctypes.byref(sh), FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == 1
+    assert L.sdm_subscores(ctypes.byref(sh), FAKE, None, FAKE, None) == 1
+    # Workspace: required, aligned and large enough.
+    need = L.sdm_workspace_size(ctypes.byref(sh))
+    assert need == sh.B * sh.H * sh.T * 16 * 2      # W + R = 16 codes of 2 bytes per token
+    assert L.sdm_scan(ctypes.byref(sh), *([FAKE] * 9), None, need, None) == 1
+    assert L.sdm_scan(ctypes.byref(sh), *([FAKE] * 9), MISALIGNED, need, None) == 1
+    assert L.sdm_scan(ctypes.byref(sh), *([FAKE] * 9), FAKE, need - 1, None) == 1
+    assert L.sdm_forward(ctypes.byref(sh), *([FAKE] * 12), FAKE, need - 1, None) == 1
+    assert L.sdm_workspace_size(ctypes.byref(good_shape(W=0))) == 0
+
+
+def test_empty_work_is_a_no_op(L):
+    # Nothing to do: returns before any CUDA call, so it works without a GPU.
+    for kw in (dict(T=0), dict(B=0), dict(H=0)):
+        sh = good_shape(**kw)
+        assert scan_rc(L, sh) == 0
+        assert L.sdm_forward(ctypes.byref(sh), *([FAKE] * 12), FAKE, 0, None) == 0
+
+
+def test_tuning_arguments(L):
+    assert L.sdm_set_scan_tuning(-1, 0) == 1
+    assert L.sdm_set_scan_tuning(17, 0) == 1
+    assert L.sdm_set_scan_tuning(4, 24) == 1
+    assert L.sdm_set_scan_tuning(4, 32) == 0
+    assert L.sdm_set_scan_tuning(0, 0) == 0
+    assert L.sdm_selftest_wait_timeout(10, None) == 1
+
+
+def test_python_binding_checks_tensors():
+    import torch
+    sh = good_shape()
+    with pytest.raises(ValueError):
+        sdm.sdm_scan(sh, *([torch.zeros(4)] * 8))

@@ -1,0 +1,328 @@
+"""CUDA path vs the CPU oracle, through the C ABI (needs an sm_103a GPU).
+
+Sizes the oracle finishes in seconds, spanning several CTA tiles and a ragged
+tail; full-size workloads are covered in test_gpu_sampled_fullsize.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests._helpers import FTOL, check_indices, gshape, max_rel, np32, oshape
+from workloads import WORKLOADS, generate
+
+pytestmark = pytest.mark.gpu
+
+sdm = pytest.importorskip("sparse_state_linear_gb300")
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sdm.lib()
+    sdm.sdm_set_scan_tuning(0, 0)
+    assert sdm.sdm_get_device_status() == 0
+    yield
+    sdm.sdm_set_scan_tuning(0, 0)
+
+
+def status_ok():
+    assert sdm.sdm_get_device_status() == 0
+
+
+# ------------------------------------------------------------------ selection
+
+def select_both(sh_o, sh_g, S_w, S_r):
+    gw = torch.from_numpy(S_w).to(DEV)
+    gr = torch.from_numpy(S_r).to(DEV)
+    idx_w, wt_w, idx_r, wt_r = sdm.sdm_select(sh_g, gw, gr)
+    status_ok()
+    ow = O.select(sh_o, 0, S_w)
+    orr = O.select(sh_o, 1, S_r)
+    return (idx_w.cpu().numpy(), wt_w.cpu().numpy(), idx_r.cpu().numpy(), wt_r.cpu().numpy()), ow, orr
+
+
+@pytest.mark.parametrize("s,W,R,kw,kr,BT", [
+    (32, 8, 8, 0, 0, (1, 37)),       # tiny shape
+    (128, 64, 64, 0, 0, (2, 23)),
+    (256, 64, 64, 0, 0, (3, 17)),    # GDN-matched
+    (512, 8, 8, 0, 0, (1, 50)),      # FwPKM-shaped
+    (256, 64, 16, 0, 0, (1, 33)),    # W != R
+    (8, 64, 64, 0, 0, (1, 19)),      # every slot selected (k = s = 8)
+    (64, 5, 3, 12, 2, (2, 21)),      # explicit k
+    (240, 64, 64, 0, 0, (1, 20)),    # non power-of-two s
+    (100, 1, 1, 0, 0, (1, 40)),      # single slot
+])
+def test_select_bit_exact_random(s, W, R, kw, kr, BT):
+    B, T = BT
+    H = 2
+    rng = np.random.default_rng(s * 131 + W)
+    S_w = rng.standard_normal((B, H, T, 2, s)).astype(np.float32)
+    S_r = (rng.standard_normal((B, H, T, 2, s)) * 3).astype(np.float32)
+    sh_o = O.Shape(B=B, H=H, T=T, n_sub=s, d_h=16, d_v=16, W=W, R=R, k_w=kw, k_r=kr)
+    sh_g = sdm.make_shape(B, H, T, s, 16, 16, W, R, k_w=kw, k_r=kr, in_dtype=sdm.SDM_F32)
+    (iw, ww, ir, wr), ow, orr = select_both(sh_o, sh_g, S_w, S_r)
+    assert np.array_equal(iw, ow[0])
+    assert np.array_equal(ir, orr[0])
+    assert np.max(np.abs(ww - ow[2])) < 2e-6
+    assert np.max(np.abs(wr - orr[2])) < 2e-6
+
+
+@pytest.mark.parametrize("kind", ["int_ties", "constant", "signed_zeros", "dominant", "huge_range",
+                                  "two_values", "neg_large"])
+def test_select_bit_exact_adversarial(kind):
+    rng = np.random.default_rng(7)
+    B, H, T, s, W = 1, 1, 48, 64, 64
+    shp = (B, H, T, 2, s)
+    if kind == "int_ties":
+        S = rng.integers(-3, 4, shp).astype(np.float32)
+    elif kind == "constant":
+        S = np.full(shp, 0.5, np.float32)
+    elif kind == "signed_zeros":
+        S = np.where(rng.random(shp) < 0.5, np.float32(0.0), np.float32(-0.0)).astype(np.float32)
+        S[..., ::7] = 1.0
+    elif kind == "dominant":
+        S = rng.standard_normal(shp).astype(np.float32)
+        S[..., 0, 5] = 1e6
+    elif kind == "huge_range":
+        S = (rng.standard_normal(shp) * 10.0 ** rng.integers(-30, 30, shp)).astype(np.float32)
+    elif kind == "two_values":
+        S = np.where(rng.random(shp) < 0.9, np.float32(1.0), np.float32(2.0))
+    else:
+        S = (-1e30 + rng.standard_normal(shp) * 1e23).astype(np.float32)
+    S_r = S[..., ::-1].copy()
+    sh_o = O.Shape(B=B, H=H, T=T, n_sub=s, d_h=16, d_v=16, W=W, R=16)
+    sh_g = sdm.make_shape(B, H, T, s, 16, 16, W, 16, in_dtype=sdm.SDM_F32)
+    (iw, ww, ir, wr), ow, orr = select_both(sh_o, sh_g, S, S_r)
+    assert np.array_equal(iw, ow[0])
+    assert np.array_equal(ir, orr[0])
+    assert np.allclose(ww, ow[2], atol=2e-6, rtol=0)
+    assert np.allclose(wr, orr[2], atol=2e-6, rtol=0)
+
+
+# ------------------------------------------------------------------ sub-scores
+
+@pytest.mark.parametrize("name", ["tiny", "mid", "gdn_matched", "fwpkm_idw"])
+def test_subscores_close_to_oracle(name):
+    w = WORKLOADS[name].with_(B=1, T=37, H=min(WORKLOADS[name].H, 2))
+    x = generate(w)
+    sh_g = gshape(w, sdm)
+    S = sdm.sdm_subscores(sh_g, x["q_w"].to(DEV), x["K"].to(DEV))
+    status_ok()
+    ref = O.subscores(oshape(w), np32(x["q_w"]), np32(x["K"]))
+    err = np.max(np.abs(np32(S) - ref))
+    assert err < 1e-5 * max(1.0, float(np.max(np.abs(ref)))), err
+
+
+# ------------------------------------------------------------------ addressing
+
+REDUCED = {
+    "tiny": dict(),
+    "mid": dict(B=1, H=2, T=203),
+    "gdn_matched": dict(B=1, H=2, T=150),
+    "fwpkm_idw": dict(B=2, T=99),
+    "long_seq": dict(H=2, T=301),
+}
+
+
+@pytest.mark.parametrize("name", list(REDUCED))
+def test_address_end_to_end(name):
+    w = WORKLOADS[name].with_(**REDUCED[name])
+    x = generate(w)
+    sh_g, sh_o = gshape(w, sdm), oshape(w)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    iw, ww, ir, wr = sdm.sdm_address(sh_g, g["q_w"], g["q_r"], g["K"])
+    status_ok()
+    iw, ww, ir, wr = (t.cpu().numpy() for t in (iw, ww, ir, wr))
+    # (1) Bit-exact given the device's own sub-scores.
+    Sg_w = np32(sdm.sdm_subscores(sh_g, g["q_w"], g["K"]))
+    Sg_r = np32(sdm.sdm_subscores(sh_g, g["q_r"], g["K"]))
+    assert np.array_equal(iw, O.select(sh_o, 0, Sg_w)[0])
+    assert np.array_equal(ir, O.select(sh_o, 1, Sg_r)[0])
+    # (2) Against the oracle's own scores: mismatches only inside the score gap.
+    S_w = O.subscores(sh_o, np32(x["q_w"]), np32(x["K"]))
+    S_r = O.subscores(sh_o, np32(x["q_r"]), np32(x["K"]))
+    ow, orr = O.select(sh_o, 0, S_w), O.select(sh_o, 1, S_r)
+    # Differences are allowed only inside the 1e-5 score gap (asserted inside).
+    check_indices(iw, ow[0], S_w, w.n_sub)
+    check_indices(ir, orr[0], S_r, w.n_sub)
+    same = np.all(iw == ow[0], axis=-1)
+    assert np.max(np.abs(ww[same] - ow[2][same])) < 1e-5
+
+
+# ------------------------------------------------------------------ scan
+
+def random_scan_case(rng, B, H, T, s, dv, W, R, bf16):
+    N = s * s
+    idx_w = np.stack([rng.choice(N, W, replace=False) for _ in range(B * H * T)])
+    idx_w = idx_w.reshape(B, H, T, W).astype(np.int32)
+    idx_r = rng.integers(0, N, (B, H, T, R)).astype(np.int32)
+    wt_w = rng.dirichlet(np.ones(W), (B, H, T)).astype(np.float32)
+    wt_r = rng.dirichlet(np.ones(R), (B, H, T)).astype(np.float32)
+    dt = torch.bfloat16 if bf16 else torch.float32
+    alpha = torch.from_numpy(rng.uniform(0.9, 1, (B, H, T)).astype(np.float32)).to(dt)
+    beta = torch.from_numpy(rng.uniform(0, 1, (B, H, T)).astype(np.float32)).to(dt)
+    v = torch.from_numpy(rng.standard_normal((B, H, T, dv)).astype(np.float32)).to(dt)
+    M0 = (rng.standard_normal((B, H, N, dv)) * 0.02).astype(np.float32)
+    return idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0
+
+
+def run_scan(sh_g, case, depth=0, cs=0):
+    idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0 = case
+    sdm.sdm_set_scan_tuning(depth, cs)
+    M = torch.from_numpy(M0).to(DEV)
+    y = sdm.sdm_scan(sh_g, torch.from_numpy(idx_w).to(DEV), torch.from_numpy(wt_w).to(DEV),
+                     torch.from_numpy(idx_r).to(DEV), torch.from_numpy(wt_r).to(DEV),
+                     alpha.to(DEV), beta.to(DEV), v.to(DEV), M)
+    status_ok()
+    sdm.sdm_set_scan_tuning(0, 0)
+    return M.cpu().numpy(), y.cpu().numpy()
+
+
+def oracle_scan(B, H, T, s, dv, W, R, case):
+    idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0 = case
+    sh = O.Shape(B=B, H=H, T=T, n_sub=s, d_h=16, d_v=dv, W=W, R=R)
+    return O.scan(sh, idx_w, wt_w.astype(np.float64), idx_r, wt_r.astype(np.float64),
+                  np32(alpha), np32(beta), np32(v), M0)
+
+
+@pytest.mark.parametrize("B,H,T,s,dv,W,R,bf16", [
+    (1, 1, 200, 8, 32, 16, 16, False),     # N=64: consecutive steps collide constantly
+    (2, 3, 150, 16, 64, 32, 48, True),
+    (1, 2, 120, 32, 128, 64, 64, True),
+    (2, 1, 90, 64, 512, 8, 8, False),
+    (1, 1, 64, 4, 16, 16, 16, False),      # W = N
+    (1, 2, 77, 8, 48, 1, 1, False),        # d_v not a multiple of 32
+])
+@pytest.mark.parametrize("depth,cs", [(1, 16), (2, 32), (4, 0), (8, 16), (16, 0)])
+def test_scan_matches_oracle(B, H, T, s, dv, W, R, bf16, depth, cs):
+    if cs == 32 and dv % 32:
+        cs = 16
+    rng = np.random.default_rng(B * 1000 + T + W)
+    case = random_scan_case(rng, B, H, T, s, dv, W, R, bf16)
+    sh_g = sdm.make_shape(B, H, T, s, 16, dv, W, R,
+                          in_dtype=sdm.SDM_BF16 if bf16 else sdm.SDM_F32)
+    Mg, yg = run_scan(sh_g, case, depth, cs)
+    Mo, yo = oracle_scan(B, H, T, s, dv, W, R, case)
+    assert max_rel(yg, yo) <= FTOL
+    assert max_rel(Mg, Mo) <= FTOL
+    # Rows no step wrote are bit-identical to the initial table.
+    idx_w, M0 = case[0], case[-1]
+    for b in range(B):
+        for h in range(H):
+            untouched = np.ones(s * s, bool)
+            untouched[idx_w[b, h].ravel()] = False
+            assert np.array_equal(Mg[b, h, untouched], M0[b, h, untouched])
+
+
+def test_scan_depth_invariance_bitwise():
+    rng = np.random.default_rng(99)
+    B, H, T, s, dv, W, R = 1, 2, 300, 8, 64, 32, 32
+    case = random_scan_case(rng, B, H, T, s, dv, W, R, True)
+    sh_g = sdm.make_shape(B, H, T, s, 16, dv, W, R, in_dtype=sdm.SDM_BF16)
+    M1, y1 = run_scan(sh_g, case, 1, 16)
+    for depth in (2, 3, 5, 8, 13):
+        M2, y2 = run_scan(sh_g, case, depth, 16)
+        assert np.array_equal(M1, M2) and np.array_equal(y1, y2), depth
+
+
+def test_scan_segments_equal_one_call():
+    rng = np.random.default_rng(5)
+    B, H, T, s, dv, W, R = 2, 2, 160, 16, 64, 16, 16
+    case = random_scan_case(rng, B, H, T, s, dv, W, R, False)
+    sh = sdm.make_shape(B, H, T, s, 16, dv, W, R, in_dtype=sdm.SDM_F32)
+    M_one, y_one = run_scan(sh, case)
+    half = sdm.make_shape(B, H, T // 2, s, 16, dv, W, R, in_dtype=sdm.SDM_F32)
+    first = tuple(np.ascontiguousarray(a[:, :, :T // 2]) if isinstance(a, np.ndarray) else
+                  a[:, :, :T // 2].contiguous() for a in case[:-1]) + (case[-1],)
+    M_a, y_a = run_scan(half, first)
+    second = tuple(np.ascontiguousarray(a[:, :, T // 2:]) if isinstance(a, np.ndarray) else
+                   a[:, :, T // 2:].contiguous() for a in case[:-1]) + (M_a,)
+    M_b, y_b = run_scan(half, second)
+    assert np.array_equal(M_one, M_b)
+    assert np.array_equal(y_one, np.concatenate([y_a, y_b], axis=2))
+
+
+# ------------------------------------------------------------------ forward
+
+@pytest.mark.parametrize("name", list(REDUCED))
+def test_forward_end_to_end(name):
+    w = WORKLOADS[name].with_(**REDUCED[name])
+    x = generate(w)
+    sh_g, sh_o = gshape(w, sdm), oshape(w)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    M = g["M0"].clone()
+    out = sdm.sdm_forward(sh_g, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M)
+    status_ok()
+    ref = O.forward(sh_o, *(np32(x[k]) for k in ("q_w", "q_r", "K", "alpha", "beta", "v")),
+                    x["M0"].numpy())
+    iw, ir = out["idx_w"].cpu().numpy(), out["idx_r"].cpu().numpy()
+    if np.array_equal(iw, ref["idx_w"]) and np.array_equal(ir, ref["idx_r"]):
+        yo, Mo = ref["y"], ref["M"]
+    else:
+        # Re-anchor: the oracle scan follows the device's selections.
+        S_w = O.subscores(sh_o, np32(x["q_w"]), np32(x["K"]))
+        S_r = O.subscores(sh_o, np32(x["q_r"]), np32(x["K"]))
+        check_indices(iw, ref["idx_w"], S_w, w.n_sub)
+        check_indices(ir, ref["idx_r"], S_r, w.n_sub)
+        Mo, yo = O.scan(sh_o, iw, np32(out["wt_w"]).astype(np.float64), ir,
+                        np32(out["wt_r"]).astype(np.float64), np32(x["alpha"]),
+                        np32(x["beta"]), np32(x["v"]), x["M0"].numpy())
+    assert max_rel(np32(out["y"]), yo) <= FTOL
+    assert max_rel(M.cpu().numpy(), Mo) <= FTOL
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_empty_inputs_are_no_ops():
+    sh = sdm.make_shape(0, 2, 5, 8, 16, 32, 4, 4, in_dtype=sdm.SDM_F32)
+    z = torch.zeros(16, device=DEV)
+    zi = torch.zeros(16, device=DEV, dtype=torch.int32)
+    sdm.sdm_scan(sh, zi, z, zi, z, z, z, z, z, y=z)
+    sh = sdm.make_shape(1, 1, 0, 8, 16, 32, 4, 4, in_dtype=sdm.SDM_F32)
+    sdm.sdm_forward(sh, z, z, z, z, z, z, z, y=z, idx_w=zi, wt_w=z, idx_r=zi, wt_r=z)
+    status_ok()
+
+
+def test_single_token_and_single_slot():
+    w = WORKLOADS["tiny"].with_(T=1, W=1, R=1)
+    x = generate(w)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    M = g["M0"].clone()
+    out = sdm.sdm_forward(gshape(w, sdm), g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"],
+                          g["v"], M)
+    status_ok()
+    ref = O.forward(oshape(w), *(np32(x[k]) for k in ("q_w", "q_r", "K", "alpha", "beta", "v")),
+                    x["M0"].numpy())
+    assert np.array_equal(out["idx_w"].cpu().numpy(), ref["idx_w"])
+    assert np.all(out["wt_w"].cpu().numpy() == 1.0)
+    assert max_rel(np32(out["y"]), ref["y"]) <= FTOL
+
+
+def test_device_detects_bad_indices():
+    B, H, T, s, dv, W, R = 1, 1, 10, 8, 32, 4, 4
+    rng = np.random.default_rng(1)
+    case = list(random_scan_case(rng, B, H, T, s, dv, W, R, False))
+    sh = sdm.make_shape(B, H, T, s, 16, dv, W, R, in_dtype=sdm.SDM_F32)
+    bad = case[0].copy()
+    bad[0, 0, 3, 1] = s * s          # out of range
+    case_b = [bad] + case[1:]
+    M = torch.from_numpy(case[-1]).to(DEV)
+    args = [torch.from_numpy(a).to(DEV) if isinstance(a, np.ndarray) else a.to(DEV)
+            for a in case_b[:-1]]
+    sdm.sdm_scan(sh, *args, M)
+    assert sdm.sdm_get_device_status() == 5
+    dup = case[0].copy()
+    dup[0, 0, 4, 2] = dup[0, 0, 4, 0]
+    args[0] = torch.from_numpy(dup).to(DEV)
+    sdm.sdm_scan(sh, *args, M)
+    assert sdm.sdm_get_device_status() == 6
+    status_ok()
+
+
+def test_bounded_wait_reports_timeout():
+    sdm.sdm_selftest_wait_timeout(50_000_000)
+    assert sdm.sdm_get_device_status() == 4
+    status_ok()

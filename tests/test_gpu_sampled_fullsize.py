@@ -1,0 +1,91 @@
+"""Full-size workloads through sdm_forward, in the launch configuration the
+benchmark times, checked on samples the oracle computes one by one:
+
+* addressing of a random sample of (b, h, t) tokens (the oracle's sub-scores
+  and selection for just those tokens);
+* the whole recurrence of sampled chains (b, h), with the oracle scan fed the
+  device's selections and weights (addressing is checked separately);
+* rows that no step of a chain wrote are bit-identical to M_0 (all chains).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests._helpers import FTOL, check_indices, gshape, max_rel, np32, oshape
+from workloads import ORDER, WORKLOADS, generate
+
+pytestmark = pytest.mark.gpu
+
+sdm = pytest.importorskip("sparse_state_linear_gb300")
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sdm.lib()
+    sdm.sdm_set_scan_tuning(0, 0)
+    assert sdm.sdm_get_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ORDER)
+def test_fullsize_forward_sampled(name):
+    w = WORKLOADS[name]
+    x = generate(w)
+    g = {k: t.to(DEV) for k, t in x.items() if k != "M0"}
+    M = x["M0"].to(DEV)
+    sh = gshape(w, sdm)
+    out = sdm.sdm_forward(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M)
+    assert sdm.sdm_get_device_status() == 0
+    iw, ir = out["idx_w"].cpu().numpy(), out["idx_r"].cpu().numpy()
+    ww, wr = out["wt_w"].cpu().numpy(), out["wt_r"].cpu().numpy()
+    rng = np.random.default_rng(1234)
+
+    # Addressing on sampled tokens: a 1 x 1 x n "sequence" of the sampled rows.
+    n = 512
+    bs = rng.integers(0, w.B, n)
+    hs = rng.integers(0, w.H, n)
+    ts = rng.integers(0, w.T, n)
+    ts[:4] = [0, w.T - 1, 0, w.T - 1]
+    for h in np.unique(hs):
+        sel = hs == h
+        m = int(sel.sum())
+        sub = O.Shape(B=1, H=1, T=m, n_sub=w.n_sub, d_h=w.d_h, d_v=w.d_v, W=w.W, R=w.R,
+                      k_w=w.k_w, k_r=w.k_r, score_kind=w.score_kind, idw_eps=w.idw_eps)
+        qw = np32(x["q_w"][bs[sel], h, ts[sel]])[None, None]
+        qr = np32(x["q_r"][bs[sel], h, ts[sel]])[None, None]
+        K = np32(x["K"][h:h + 1])
+        S_w, S_r = O.subscores(sub, qw, K), O.subscores(sub, qr, K)
+        ow, orr = O.select(sub, 0, S_w), O.select(sub, 1, S_r)
+        gw = iw[bs[sel], h, ts[sel]][None, None]
+        gr = ir[bs[sel], h, ts[sel]][None, None]
+        # Differences are allowed only inside the 1e-5 score gap (asserted inside).
+        check_indices(gw, ow[0], S_w, w.n_sub)
+        check_indices(gr, orr[0], S_r, w.n_sub)
+        same = np.all(gw == ow[0], axis=-1)
+        assert np.max(np.abs(ww[bs[sel], h, ts[sel]][None, None][same] - ow[2][same])) < 1e-5
+
+    # Whole chains: the oracle recurrence on the device's selections.
+    Mg = M  # updated in place on the device
+    chains = [(0, 0), (w.B - 1, w.H - 1)] if w.B * w.H > 1 else [(0, 0)]
+    for b, h in chains:
+        one = O.Shape(B=1, H=1, T=w.T, n_sub=w.n_sub, d_h=w.d_h, d_v=w.d_v, W=w.W, R=w.R)
+        Mo, yo = O.scan(one, iw[b:b + 1, h:h + 1], ww[b:b + 1, h:h + 1].astype(np.float64),
+                        ir[b:b + 1, h:h + 1], wr[b:b + 1, h:h + 1].astype(np.float64),
+                        np32(x["alpha"][b:b + 1, h:h + 1]), np32(x["beta"][b:b + 1, h:h + 1]),
+                        np32(x["v"][b:b + 1, h:h + 1]), x["M0"][b:b + 1, h:h + 1].numpy())
+        yg = out["y"][b, h].cpu().numpy()
+        assert max_rel(yg, yo[0, 0]) <= FTOL
+        assert max_rel(Mg[b, h].cpu().numpy(), Mo[0, 0]) <= FTOL
+
+    # Untouched rows, every chain (checked on the device, bitwise).
+    for b in range(w.B):
+        for h in range(w.H):
+            touched = torch.zeros(w.N, dtype=torch.bool, device=DEV)
+            touched[out["idx_w"][b, h].reshape(-1).long()] = True
+            M0bh = x["M0"][b, h].to(DEV)
+            assert torch.equal(Mg[b, h][~touched], M0bh[~touched])
+    del g, M, out
+    torch.cuda.empty_cache()

@@ -1,0 +1,375 @@
+"""Benchmark of the SDM forward step (addressing + scan) on GB300.
+
+One step = one sdm_forward over one batch of the workload (default
+``gdn_matched``: B=8, H=8, T=4096, N=65536 slots, W=R=64, d_v=128, bf16
+inputs, fp32 table of 2 GiB).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain C++ restatement of the
+method) on this machine's host cores, on a bounded sample of the same workload.
+Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, generate  # noqa: E402
+
+METRIC = "SDM forward tokens/s on 1 GB300; scan-kernel GB/s as % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def scan_bytes_per_token_head(w) -> int:
+    """Algorithmic bytes the scan must move per token-head: W rows read and
+    written, R rows read (d_v fp32 each), v and the two gates (input dtype),
+    slot indices and weights (8 B per slot), and y (d_v fp32)."""
+    ib = 2 if w.bf16 else 4
+    return (2 * w.W + w.R) * w.d_v * 4 + w.d_v * ib + 2 * ib + (w.W + w.R) * 8 + w.d_v * 4
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed work runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, pw = [], [], []
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        # Samples under load: power within 40% of the highest seen.
+        hi = max(pw) if pw else 0.0
+        load = [s for s, p in zip(sm, pw) if p >= 0.6 * hi] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(load)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def traffic_for(kernel_src: str):
+    """DRAM bytes per scan launch recorded by an ncu capture of this exact
+    kernel source (profiles/traffic.json keyed by the source's sha256);
+    None if the kernel changed since."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+        with open(kernel_src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+        ent = rec.get(h)
+        return None if ent is None else float(ent["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def oracle_sample_rate(w, budget_s: float, seed_offset: int = 0):
+    """Time the CPU oracle (single thread) on chain (0, 0) of the workload,
+    growing the token count until about `budget_s` seconds of work.  Returns
+    (equivalent tokens/s of the whole workload, description)."""
+    import oracle as O
+    T = 64
+    spent = 0.0
+    last = None
+    while True:
+        ws = w.with_(B=1, H=1, T=T, seed=w.seed + seed_offset)
+        x = generate(ws)
+        sh = O.Shape(1, 1, T, w.n_sub, w.d_h, w.d_v, w.W, w.R, k_w=w.k_w, k_r=w.k_r,
+                     score_kind=w.score_kind, idw_eps=w.idw_eps, update_form=w.update_form)
+        args = [x[k].float().numpy() for k in ("q_w", "q_r", "K", "alpha", "beta", "v")]
+        t0 = time.perf_counter()
+        O.forward(sh, *args, x["M0"].numpy())
+        dt = time.perf_counter() - t0
+        spent += dt
+        last = (T, dt)
+        if spent >= budget_s or T >= w.T or dt * 2 > budget_s - spent:
+            break
+        T = min(w.T, T * 2)
+    T, dt = last
+    # One token of the workload is H token-heads (all heads of the token).
+    tok_per_s = (T / dt) / w.H
+    desc = (f"oracle forward (subscores, selection, scan) of chain (b=0,h=0), first {T} of "
+            f"{w.T} tokens, {dt:.2f} s on 1 thread; rate scaled to tokens of all {w.H} heads")
+    return tok_per_s, desc, T, dt
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle as O
+    O.build()
+    steps, warm = args.steps, args.warmup
+    # Per-step sample sized so the whole run stays within ~2 minutes.
+    calib_rate, _, _, _ = oracle_sample_rate(w, 2.0)
+    per_step_s = max(0.05, 120.0 / max(1, steps + warm))
+    T = max(8, min(w.T, int(calib_rate * w.H * per_step_s)))
+    sample = w.with_(B=1, H=1, T=T)
+    x = generate(sample)
+    sh = O.Shape(1, 1, T, w.n_sub, w.d_h, w.d_v, w.W, w.R, k_w=w.k_w, k_r=w.k_r,
+                 score_kind=w.score_kind, idw_eps=w.idw_eps, update_form=w.update_form)
+    arrays = [x[k].float().numpy() for k in ("q_w", "q_r", "K", "alpha", "beta", "v")]
+    for _ in range(warm):
+        O.forward(sh, *arrays, x["M0"].numpy())
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        O.forward(sh, *arrays, x["M0"].numpy())
+    el = time.perf_counter() - t0
+    tok_per_s = (steps * T / w.H) / el
+    desc = (f"per step: oracle forward of one chain, {T} tokens ({T} token-heads) of the "
+            f"{w.name} workload on 1 thread; rate scaled to tokens of all {w.H} heads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok_per_s, "unit": "tokens/s",
+        "n_gpus": ws, "steps": steps, "warmup": warm,
+        "ms_per_step": el / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": tok_per_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": tok_per_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "N": w.N, "n_sub": w.n_sub,
+            "d_h": w.d_h, "d_v": w.d_v, "W": w.W, "R": w.R,
+            "inputs": "bf16" if w.bf16 else "f32", "state": "f32",
+            "score": "dot" if w.score_kind == 0 else "inverse-distance",
+            "global_batch": w.B, "seq_len": w.T,
+            "l2": f"inputs larger than L2 (fp32 table {w.B * w.H * w.N * w.d_v * 4 / 2**30:.2f} GiB)"}
+
+
+def run_ours(args, w):
+    import sparse_state_linear_gb300 as sdm
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    sdm.lib()
+    # Each rank draws its own batch (weak scaling).
+    wr = w.with_(seed=w.seed + 1000 * rank) if rank else w
+    x = generate(wr)
+    g = {k: t.to(dev) for k, t in x.items() if k != "M0"}
+    M = x["M0"].to(dev)
+    del x
+    sh = sdm.make_shape(w.B, w.H, w.T, w.n_sub, w.d_h, w.d_v, w.W, w.R, k_w=w.k_w, k_r=w.k_r,
+                        in_dtype=sdm.SDM_BF16 if w.bf16 else sdm.SDM_F32, score=w.score_kind,
+                        idw_eps=w.idw_eps, update=w.update_form)
+    BHT = (w.B, w.H, w.T)
+    y = torch.empty(BHT + (w.d_v,), dtype=torch.float32, device=dev)
+    idx_w = torch.empty(BHT + (w.W,), dtype=torch.int32, device=dev)
+    idx_r = torch.empty(BHT + (w.R,), dtype=torch.int32, device=dev)
+    wt_w = torch.empty(BHT + (w.W,), dtype=torch.float32, device=dev)
+    wt_r = torch.empty(BHT + (w.R,), dtype=torch.float32, device=dev)
+    wsp = torch.empty(max(16, sdm.sdm_workspace_size(sh)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def forward():
+        sdm.sdm_forward(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M, y,
+                        idx_w, wt_w, idx_r, wt_r, workspace=wsp, stream=stream)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        forward()
+    torch.cuda.synchronize(dev)
+    if sdm.sdm_get_device_status(stream) != 0:
+        raise RuntimeError("device reported a failure during warm-up")
+
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[dev.index]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else dev.index
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    with ClockSampler(gpu_index) as clk:
+        # ---- the timed region: K full forward steps.
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(args.steps):
+            forward()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        ms = e0.elapsed_time(e1)
+        if ws > 1:
+            import torch.distributed as dist
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        status = sdm.sdm_get_device_status(stream)
+
+        # ---- per-kernel durations (same stream, events around each call).
+        def per_call(fn, n):
+            evs = [(ev(), ev()) for _ in range(n)]
+            for a, b in evs:
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            return sum(a.elapsed_time(b) for a, b in evs) / n
+
+        nk = max(3, min(args.steps, 20))
+        t_addr = per_call(lambda: sdm.sdm_address(sh, g["q_w"], g["q_r"], g["K"], idx_w, wt_w,
+                                                  idx_r, wt_r, stream=stream), nk)
+        t_scan = per_call(lambda: sdm.sdm_scan(sh, idx_w, wt_w, idx_r, wt_r, g["alpha"],
+                                               g["beta"], g["v"], M, y, workspace=wsp,
+                                               stream=stream), nk)
+
+        # ---- end to end through the public API with host buffers.
+        host = {k: g[k].cpu().pin_memory() for k in ("q_w", "q_r", "alpha", "beta", "v")}
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = y_host.numel() * y_host.element_size()
+        ne = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            for k, t in host.items():
+                g[k].copy_(t, non_blocking=True)
+            forward()
+            y_host.copy_(y, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(ne):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b) / ne
+    if status != 0:
+        raise RuntimeError(f"device reported status {status} in the timed region")
+
+    tokens = w.B * w.T
+    value = tokens * ws * args.steps / (ms / 1e3)
+    peak, peak_kind = measured_peaks()
+    bytes_launch = scan_bytes_per_token_head(w) * w.B * w.H * w.T
+    achieved = bytes_launch / (t_scan / 1e3) / 1e9
+    traffic = traffic_for(os.path.join(ROOT, "sparse_state_linear_gb300", "csrc", "scan.cu"))
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; bf16 inputs, fp32 table)" if w.bf16 else "synthetic (seeded, fp32)",
+        "config": dict(config_of(w), parallelism=f"dp{ws}" if ws > 1 else "single"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "sdm_scan (plan + scan kernels)",
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": bytes_launch},
+        "kernels_ms": {"sdm_address": t_addr, "sdm_scan": t_scan},
+        "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if ws == 1 and rank == 0 and not args.no_cpu_baseline:
+        rate, desc, _, _ = oracle_sample_rate(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gdn_matched", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -115,6 +115,26 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_workload(w, rank: int):
+    """Each rank runs its own batch of the same shape (weak scaling)."""
+    return w.with_(seed=w.seed + 1000 * rank) if rank else w
+
+
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time: the job's time."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank_step: int, world: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: tokens of all ranks over the max-over-ranks time."""
+    return tokens_per_rank_step * world * steps / (ms / 1e3)
+
+
 def traffic_for(kernel_src: str):
     """DRAM bytes per scan launch recorded by an ncu capture of this exact
     kernel source (profiles/traffic.json keyed by the source's sha256);
@@ -219,9 +239,7 @@ def run_ours(args, w):
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     sdm.lib()
-    # Each rank draws its own batch (weak scaling).
-    wr = w.with_(seed=w.seed + 1000 * rank) if rank else w
-    x = generate(wr)
+    x = generate(rank_workload(w, rank))
     g = {k: t.to(dev) for k, t in x.items() if k != "M0"}
     M = x["M0"].to(dev)
     del x
@@ -266,12 +284,7 @@ def run_ours(args, w):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-        ms = e0.elapsed_time(e1)
-        if ws > 1:
-            import torch.distributed as dist
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(e0.elapsed_time(e1), dev)
         status = sdm.sdm_get_device_status(stream)
 
         # ---- per-kernel durations (same stream, events around each call).
@@ -318,7 +331,7 @@ def run_ours(args, w):
         raise RuntimeError(f"device reported status {status} in the timed region")
 
     tokens = w.B * w.T
-    value = tokens * ws * args.steps / (ms / 1e3)
+    value = job_tokens_per_s(tokens, ws, args.steps, ms)
     peak, peak_kind = measured_peaks()
     bytes_launch = scan_bytes_per_token_head(w) * w.B * w.H * w.T
     achieved = bytes_launch / (t_scan / 1e3) / 1e9

@@ -132,6 +132,28 @@ sdm_status sdm_scan(const sdm_shape* shape, const int32_t* idx_w,
                     float* M, float* y, void* workspace, size_t ws_bytes,
                     void* stream);
 
+/* sdm_scan without a workspace, for callers that cannot allocate device
+ * memory: e.g. a host framework that owns all device memory and only passes
+ * in the tensors of a call, or a code path where a cudaMalloc (and the
+ * device-wide synchronisation it may bring) is not allowed.  The paper has no
+ * counterpart; this is an interface variant of sdm_scan, same arguments and
+ * results minus `workspace`/`ws_bytes`.
+ * Scratch: a fixed 8 MiB array of device memory in the library itself (every
+ * GPU that loads the library holds it until the process exits).  Problems
+ * needing more plan-code scratch than that, i.e.
+ * B*H*T*round_up(W+R, 8)*2 bytes > 8 MiB (32768 token-heads at W = R = 64),
+ * return SDM_ERR_UNSUPPORTED before anything is enqueued.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the one array: calls whose work overlaps on the GPU (other streams,
+ * other threads) race and must be serialised by the caller.  Nothing in the
+ * array needs clearing: every value a call reads, that call wrote first.
+ * Calls no cudaMalloc, cudaFree or allocating library routine. */
+sdm_status sdm_scan_noalloc(const sdm_shape* shape, const int32_t* idx_w,
+                            const float* wt_w, const int32_t* idx_r,
+                            const float* wt_r, const void* alpha, const void* beta,
+                            const void* v, float* M, float* y, void* stream);
+
 /* One full forward step: sdm_address then sdm_scan on `stream`.
  * Inputs as above; M updated in place, y written, and the selected indices
  * and weights returned in the caller's idx_w/wt_w/idx_r/wt_r buffers. */

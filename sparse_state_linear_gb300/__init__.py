@@ -25,7 +25,8 @@ STATUS = {0: "SDM_OK", 1: "SDM_ERR_INVALID_ARG", 2: "SDM_ERR_UNSUPPORTED", 3: "S
           4: "SDM_ERR_TIMEOUT", 5: "SDM_ERR_DEVICE_BOUNDS", 6: "SDM_ERR_DUPLICATE_SLOT"}
 
 EXPORTS = ["sdm_status_string", "sdm_subscores", "sdm_select", "sdm_address",
-           "sdm_workspace_size", "sdm_scan", "sdm_forward", "sdm_get_device_status",
+           "sdm_workspace_size", "sdm_scan", "sdm_scan_noalloc", "sdm_forward",
+           "sdm_get_device_status",
            "sdm_set_scan_tuning", "sdm_selftest_wait_timeout"]
 
 
@@ -83,6 +84,7 @@ def lib():
         "sdm_address": ([SP, P, P, P, P, P, P, P, P], I),
         "sdm_workspace_size": ([SP], ctypes.c_size_t),
         "sdm_scan": ([SP] + [P] * 10 + [ctypes.c_size_t, P], I),
+        "sdm_scan_noalloc": ([SP] + [P] * 10, I),
         "sdm_forward": ([SP] + [P] * 13 + [ctypes.c_size_t, P], I),
         "sdm_get_device_status": ([P], I),
         "sdm_set_scan_tuning": ([I, I], I),
@@ -200,6 +202,21 @@ def sdm_scan(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y=None, wor
                        _ptr(alpha, "alpha", dt), _ptr(beta, "beta", dt), _ptr(v, "v", dt),
                        _ptr(M, "M", f32), _ptr(y, "y", f32), _ptr(ws, "workspace"), nws,
                        _stream(stream)), "sdm_scan")
+    return y
+
+
+def sdm_scan_noalloc(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y=None,
+                     stream=None):
+    """sdm_scan with the library's fixed scratch instead of a workspace (for
+    callers that cannot allocate); M updated in place; returns y."""
+    if y is None:
+        y = _empty((sh.B, sh.H, sh.T, sh.d_v), torch.float32, M)
+    dt, f32, i32 = _in_dt(sh), (torch.float32,), (torch.int32,)
+    _ok(lib().sdm_scan_noalloc(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32),
+                               _ptr(wt_w, "wt_w", f32), _ptr(idx_r, "idx_r", i32),
+                               _ptr(wt_r, "wt_r", f32), _ptr(alpha, "alpha", dt),
+                               _ptr(beta, "beta", dt), _ptr(v, "v", dt), _ptr(M, "M", f32),
+                               _ptr(y, "y", f32), _stream(stream)), "sdm_scan_noalloc")
     return y
 
 

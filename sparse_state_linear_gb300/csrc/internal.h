@@ -41,4 +41,9 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
                         const void* beta, const void* v, float* M, float* y, void* workspace,
                         int depth, int col_slice, unsigned* status, cudaStream_t stream);
 
+// Accessors of the API layer (sdm_api.cu) for other entry points.
+sdm_status api_check_shape(const sdm_shape* shape, Dims* d);
+sdm_status api_status_ptr(unsigned** out);
+void api_scan_tuning(int* depth, int* col_slice);
+
 }  // namespace sdm

@@ -99,6 +99,15 @@ __global__ void wait_timeout_selftest(unsigned* status, unsigned long long timeo
 }
 
 }  // namespace
+
+sdm_status api_check_shape(const sdm_shape* shape, Dims* d) { return check_shape(shape, d); }
+sdm_status api_status_ptr(unsigned** out) { return status_ptr(out); }
+void api_scan_tuning(int* depth, int* col_slice) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  *depth = g_depth;
+  *col_slice = g_colslice;
+}
+
 }  // namespace sdm
 
 using namespace sdm;

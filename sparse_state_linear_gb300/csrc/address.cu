@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads) address_kernel(const AddrArgs A) {
       if (item >= BT) continue;
       const int k = sg == 0 ? d.kw : d.kr;
       RowSrc src{sc + (size_t)r * d.s};
-      warp_topk_sorted(src, d.s, k, ws, lane);
+      warp_topk<16>(src, d.s, k, ws, lane);
       float* ov = lv + (r * 2 + p) * kMaxSel;
       uint32_t* oi = lid + (r * 2 + p) * kMaxSel;
       for (int e = lane; e < k; e += 32) {

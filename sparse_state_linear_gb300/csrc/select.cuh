@@ -40,10 +40,21 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+constexpr int kTmpCap = 128;   // bucket-ordered candidates of the fast path
+
 struct WarpScratch {
-  uint32_t hist[256];
-  float cand_v[kMaxSel];
-  uint32_t cand_id[kMaxSel];
+  uint32_t hist[256];          // digit / bucket counts; fast path: then scatter cursors
+  uint32_t base[260];          // fast path: exclusive prefix of bucket counts
+  union {
+    struct {                   // radix path: unsorted winners
+      float cand_v[kMaxSel];
+      uint32_t cand_id[kMaxSel];
+    };
+    struct {                   // fast path: candidates in bucket order
+      float tmp_v[kTmpCap];
+      uint32_t tmp_id[kTmpCap];
+    };
+  };
   float out_v[kMaxSel];
   uint32_t out_id[kMaxSel];
 };
@@ -238,6 +249,120 @@ __device__ void warp_topk_sorted(const Src& src, int n, int k, WarpScratch& ws, 
   __syncwarp();
 }
 
+// Fast exact top-k for n <= 32*PL elements (values cached in registers).
+// One pass buckets every value by its distance below the row maximum:
+// bucket(v) = min(255, trunc((vmax - v) * 256 / (vmax - vmin))).  The map is
+// monotone and equal values share a bucket, so an element in a lower bucket
+// is strictly larger than any element in a higher one.  Buckets up to the one
+// holding the k-th element are scattered in bucket order (counting sort) and
+// every candidate's rank is its bucket's base plus the number of members of
+// its own bucket that come first in (value desc, id asc).  Returns false
+// (nothing written) when the data defeat the bucketing (all values equal, an
+// infinite range, or more than kTmpCap candidates up to the boundary bucket);
+// the caller then uses warp_topk_sorted.
+template <int PL, class Src>
+__device__ bool warp_topk_bucketed(const Src& src, int n, int k, WarpScratch& ws, int lane) {
+  float v[PL];
+  float vmax = -INFINITY, vmin = INFINITY;
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = 0.f;
+    if (e < n) {
+      uint32_t id;
+      src.get(e, v[i], id);
+      vmax = fmaxf(vmax, v[i]);
+      vmin = fminf(vmin, v[i]);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, off));
+    vmin = fminf(vmin, __shfl_xor_sync(kFull, vmin, off));
+  }
+  const float range = vmax - vmin;
+  if (!(range > 0.f) || !(range < INFINITY)) return false;
+  const float scale = 256.f / range;
+  auto bucket = [&](float x) -> uint32_t {
+    const float dd = (vmax - x) * scale;
+    return min(255u, __float2uint_rz(dd));
+  };
+  for (int i = lane; i < 256; i += 32) ws.hist[i] = 0u;
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < PL; ++i)
+    if (lane + 32 * i < n) atomicAdd(&ws.hist[bucket(v[i])], 1u);
+  __syncwarp();
+  // Exclusive prefix over buckets (lane owns 8 consecutive buckets).
+  uint32_t c[8], tot = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    c[i] = ws.hist[8 * lane + i];
+    tot += c[i];
+  }
+  uint32_t inc = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(kFull, inc, off);
+    if (lane >= off) inc += t;
+  }
+  uint32_t run = inc - tot;
+  uint32_t bstar = 256;          // boundary bucket (found by exactly one lane)
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    ws.base[8 * lane + i] = run;
+    ws.hist[8 * lane + i] = run;   // from here on: scatter cursors
+    if (run < (uint32_t)k && (uint32_t)k <= run + c[i]) bstar = 8 * lane + i;
+    run += c[i];
+  }
+  if (lane == 31) ws.base[256] = run;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) bstar = min(bstar, __shfl_xor_sync(kFull, bstar, off));
+  __syncwarp();
+  const uint32_t ncand = ws.base[bstar + 1];
+  if (ncand > (uint32_t)kTmpCap) return false;
+  // Scatter the candidates in bucket order.
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < n) {
+      const uint32_t b = bucket(v[i]);
+      if (b <= bstar) {
+        float vv;
+        uint32_t id;
+        src.get(e, vv, id);
+        const uint32_t pos = atomicAdd(&ws.hist[b], 1u);
+        ws.tmp_v[pos] = v[i];
+        ws.tmp_id[pos] = id;
+      }
+    }
+  }
+  __syncwarp();
+  // Exact rank of every candidate; the best k land in ws.out_* in order.
+  for (uint32_t p = lane; p < ncand; p += 32) {
+    const float pv = ws.tmp_v[p];
+    const uint32_t pid = ws.tmp_id[p];
+    const uint32_t b = bucket(pv);
+    const uint32_t lo = ws.base[b], hi = ws.base[b + 1];
+    uint32_t r = lo;
+    for (uint32_t q = lo; q < hi; ++q) r += better(ws.tmp_v[q], ws.tmp_id[q], pv, pid) ? 1u : 0u;
+    if (r < (uint32_t)k) {
+      ws.out_v[r] = pv;
+      ws.out_id[r] = pid;
+    }
+  }
+  __syncwarp();
+  return true;
+}
+
+// Best k of n (k <= 64): the bucketed path when it applies, else the radix one.
+template <int PL, class Src>
+__device__ __forceinline__ void warp_topk(const Src& src, int n, int k, WarpScratch& ws, int lane) {
+  if (n <= 32 * PL && warp_topk_bucketed<PL>(src, n, k, ws, lane)) return;
+  warp_topk_sorted(src, n, k, ws, lane);
+}
+
 // Element sources ------------------------------------------------------------
 
 // One half's sub-scores: element j has value row[j] and id j.
@@ -311,7 +436,7 @@ __device__ __forceinline__ void warp_merge(const float* v1, const uint32_t* id1,
                                            int nsel, uint32_t s, const uint16_t* stair,
                                            int nstair, WarpScratch& ws, int lane) {
   PairSrc ps{v1, id1, v2, id2, stair, s};
-  warp_topk_sorted(ps, nstair, nsel, ws, lane);
+  warp_topk<10>(ps, nstair, nsel, ws, lane);
   const float cw = ws.out_v[nsel - 1];
   bool tie = false;
   for (int a = lane; a < k; a += 32) {

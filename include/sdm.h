@@ -169,7 +169,7 @@ sdm_status sdm_get_device_status(void* stream);
 
 /* Scan launch tuning for the calling process (0 = automatic):
  *   depth      steps whose rows are in flight per chain slice, 1..16;
- *   col_slice  columns of d_v per CTA, 16 or 32 (must divide d_v).
+ *   col_slice  columns of d_v per CTA, 16, 32 or 64 (must divide d_v).
  * Results do not depend on these; only speed does. */
 sdm_status sdm_set_scan_tuning(int depth, int col_slice);
 

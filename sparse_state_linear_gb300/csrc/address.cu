@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "select.cuh"
+#include "tcgen05.cuh"
 
 namespace sdm {
 namespace {
@@ -315,8 +316,234 @@ cudaError_t launch_t(const AddrArgs& A, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ tensor cores
+// bf16 dot-product scores on the 5th-generation tensor cores.  One CTA =
+// one head x 128 MMA rows (64 tokens x 2 branches when fused, 128 tokens of
+// one branch for scores only).  Both halves' contractions (128 x d_h by
+// d_h x s, fp32 accumulate) are issued by one thread into 2 x 256 tensor-
+// memory columns; rows are then staged 32 at a time through padded shared
+// memory for the warp selection and merge above.
+constexpr int kTcRows = 128;
+constexpr int kTcThreads = 512;
+
+struct TcLayout {
+  size_t a, b, sc, lv, lid, ws, stair, nst, bar, tslot, total;
+  int spad, scs;
+};
+
+__host__ __device__ inline TcLayout tc_layout(int s, int dh) {
+  TcLayout L;
+  L.spad = (s + 15) & ~15;     // MMA N
+  L.scs = L.spad + 4;          // staged row stride in floats (16-byte rows, no bank conflicts)
+  size_t o = 0;
+  L.a = o;     o = align_up(o + (size_t)2 * kTcRows * dh * 2, 1024);
+  L.b = o;     o = align_up(o + (size_t)2 * L.spad * dh * 2, 1024);
+  L.sc = o;    o = align_up(o + sizeof(float) * 32 * (size_t)L.scs, 16);
+  L.lv = o;    o = align_up(o + sizeof(float) * 32 * 2 * kMaxSel, 16);
+  L.lid = o;   o = align_up(o + sizeof(uint32_t) * 32 * 2 * kMaxSel, 16);
+  L.ws = o;    o = align_up(o + sizeof(WarpScratch) * (kTcThreads / 32), 16);
+  L.stair = o; o = align_up(o + sizeof(uint16_t) * 2 * kStairMax, 16);
+  L.nst = o;   o = align_up(o + sizeof(int) * 2, 16);
+  L.bar = o;   o = align_up(o + sizeof(uint64_t), 16);
+  L.tslot = o; o = align_up(o + sizeof(uint32_t), 16);
+  L.total = o;
+  return L;
+}
+
+inline bool tc_eligible(const Dims& d) {
+  return d.in_dtype == SDM_BF16 && d.score == SDM_SCORE_DOT && d.s <= 256 && d.dh <= 64 &&
+         d.dh % 16 == 0 && tc_layout(d.s, d.dh).total <= 232448;
+}
+
+template <int MODE>
+__device__ __forceinline__ void tc_row_item(int r, int& sigma, long long& item) {
+  if (MODE == kAddrScoresOnly) {
+    sigma = 0;
+    item = (long long)blockIdx.x * kTcRows + r;
+  } else {
+    sigma = r >> 6;
+    item = (long long)blockIdx.x * (kTcRows / 2) + (r & 63);
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArgs A) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const Dims& d = A.d;
+  const TcLayout L = tc_layout(d.s, d.dh);
+  unsigned char* sA = smem + L.a;
+  unsigned char* sB = smem + L.b;
+  float* sc = reinterpret_cast<float*>(smem + L.sc);
+  float* lv = reinterpret_cast<float*>(smem + L.lv);
+  uint32_t* lid = reinterpret_cast<uint32_t*>(smem + L.lid);
+  WarpScratch* wsa = reinterpret_cast<WarpScratch*>(smem + L.ws);
+  uint16_t* stair = reinterpret_cast<uint16_t*>(smem + L.stair);
+  int* nst = reinterpret_cast<int*>(smem + L.nst);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L.tslot);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y, dh = d.dh, spad = L.spad, scs = L.scs;
+  const long long BT = (long long)d.B * d.T;
+  const uint32_t ahalf = (uint32_t)kTcRows * dh * 2, bhalf = (uint32_t)spad * dh * 2;
+  // Tensor-memory columns: half p's accumulators start at column p * cstride.
+  const uint32_t cstride = spad <= 128 ? 128u : 256u, ncols = 2 * cstride;
+  WarpScratch& ws = wsa[warp];
+
+  if (warp == 0) tc::tmem_alloc(tslot, ncols);
+  if (tid == 32) mbar_init(bar, 1);
+  if (MODE != kAddrScoresOnly) {
+    if (warp == 2) {
+      const int n = build_stair(d.W, d.kw, stair, lane);
+      if (lane == 0) nst[0] = n;
+    } else if (warp == 3) {
+      const int n = build_stair(d.R, d.kr, stair + kStairMax, lane);
+      if (lane == 0) nst[1] = n;
+    }
+  }
+  // Operands into the K-major core-matrix layout (16-byte chunks).
+  const int kc = dh / 8;
+  for (int e = tid; e < 2 * kTcRows * kc; e += kTcThreads) {
+    const int p = e / (kTcRows * kc), rem = e - p * kTcRows * kc;
+    const int r = rem / kc, c = rem - r * kc;
+    int sg;
+    long long item;
+    tc_row_item<MODE>(r, sg, item);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (item < BT) {
+      const long long b = item / d.T, t = item - b * d.T;
+      const long long th = (b * d.H + h) * d.T + t;
+      const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(sg == 0 ? A.q0 : A.q1);
+      v = __ldg(reinterpret_cast<const uint4*>(q + (size_t)(th * 2 + p) * dh) + c);
+    }
+    *reinterpret_cast<uint4*>(sA + p * ahalf + tc::kmajor_off(r, 8 * c, dh)) = v;
+  }
+  for (int e = tid; e < 2 * spad * kc; e += kTcThreads) {
+    const int p = e / (spad * kc), rem = e - p * spad * kc;
+    const int j = rem / kc, c = rem - j * kc;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (j < d.s) {
+      const __nv_bfloat16* K = reinterpret_cast<const __nv_bfloat16*>(A.K);
+      v = __ldg(reinterpret_cast<const uint4*>(K + ((size_t)(h * 2 + p) * d.s + j) * dh) + c);
+    }
+    *reinterpret_cast<uint4*>(sB + p * bhalf + tc::kmajor_off(j, 8 * c, dh)) = v;
+  }
+  tc::fence_smem_to_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  if (tid == 0) {
+    const uint32_t idesc = tc::idesc_bf16_f32(kTcRows, spad);
+    const uint32_t sbo = (uint32_t)dh * 16;
+    for (int p = 0; p < 2; ++p)
+      for (int ks = 0; ks < dh / 16; ++ks)
+        tc::mma_bf16(tmem + p * cstride,
+                     tc::kmajor_desc(smem_u32(sA + p * ahalf) + ks * 256, 128, sbo),
+                     tc::kmajor_desc(smem_u32(sB + p * bhalf) + ks * 256, 128, sbo), idesc,
+                     ks > 0);
+    tc::commit(bar);
+  }
+  if (!mbar_wait_bounded(bar, 0, 4000000000ull)) record_status(A.status, SDM_ERR_TIMEOUT);
+  tc::fence_after_sync();
+
+  if (MODE == kAddrScoresOnly) {
+    // Warps 0-3: half 0, warps 4-7: half 1; lane = row.
+    const int g = warp & 3, p = (warp >> 2) & 1;
+    const int r = 32 * g + lane;
+    int sg;
+    long long item;
+    tc_row_item<MODE>(r, sg, item);
+    long long th = 0;
+    if (item < BT) {
+      const long long b = item / d.T, t = item - b * d.T;
+      th = (b * d.H + h) * d.T + t;
+    }
+    // Warps 8-15 take the second half of the columns.
+    for (int c0 = 16 * (warp >> 3); c0 < spad; c0 += 32) {
+      float v[16];
+      tc::ld16(tmem + ((uint32_t)(32 * g) << 16) + p * cstride + c0, v);
+      if (item < BT)
+        for (int i = 0; i < 16; ++i)
+          if (c0 + i < d.s) A.S[(size_t)(th * 2 + p) * d.s + c0 + i] = v[i];
+    }
+  } else {
+    for (int g = 0; g < 4; ++g) {
+      for (int p = 0; p < 2; ++p) {
+        // Stage rows 32g .. 32g+31 of half p (warps g and g+4 share the columns).
+        if ((warp & 3) == g) {
+          for (int blk = warp >> 2; blk < spad / 16; blk += kTcThreads / 128) {
+            float v[16];
+            tc::ld16(tmem + ((uint32_t)(32 * g) << 16) + p * cstride + 16 * blk, v);
+            float4* dst = reinterpret_cast<float4*>(sc + (size_t)lane * scs + 16 * blk);
+            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+            dst[2] = make_float4(v[8], v[9], v[10], v[11]);
+            dst[3] = make_float4(v[12], v[13], v[14], v[15]);
+          }
+        }
+        __syncthreads();
+        for (int rr = warp; rr < 32; rr += kTcThreads / 32) {
+          int sg;
+          long long item;
+          tc_row_item<MODE>(32 * g + rr, sg, item);
+          if (item >= BT) continue;
+          const int k = sg == 0 ? d.kw : d.kr;
+          RowSrc src{sc + (size_t)rr * scs};
+          warp_topk<16>(src, d.s, k, ws, lane);
+          float* ov = lv + (rr * 2 + p) * kMaxSel;
+          uint32_t* oi = lid + (rr * 2 + p) * kMaxSel;
+          for (int e = lane; e < k; e += 32) {
+            ov[e] = ws.out_v[e];
+            oi[e] = ws.out_id[e];
+          }
+          __syncwarp();
+        }
+        __syncthreads();
+      }
+      for (int rr = warp; rr < 32; rr += kTcThreads / 32) {
+        int sg;
+        long long item;
+        tc_row_item<MODE>(32 * g + rr, sg, item);
+        if (item >= BT) continue;
+        const int k = sg == 0 ? d.kw : d.kr;
+        const int nsel = sg == 0 ? d.W : d.R;
+        warp_merge(lv + (rr * 2 + 0) * kMaxSel, lid + (rr * 2 + 0) * kMaxSel,
+                   lv + (rr * 2 + 1) * kMaxSel, lid + (rr * 2 + 1) * kMaxSel, k, nsel,
+                   (uint32_t)d.s, stair + sg * kStairMax, nst[sg], ws, lane);
+        const long long b = item / d.T, t = item - b * d.T;
+        const long long th = (b * d.H + h) * d.T + t;
+        int32_t* io = (sg == 0 ? A.idx_w : A.idx_r) + (size_t)th * nsel;
+        float* wo = (sg == 0 ? A.wt_w : A.wt_r) + (size_t)th * nsel;
+        warp_softmax_store(ws, nsel, io, wo, lane);
+        __syncwarp();
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, ncols);
+}
+
+template <int MODE>
+cudaError_t launch_tc(const AddrArgs& A, cudaStream_t stream) {
+  const TcLayout L = tc_layout(A.d.s, A.d.dh);
+  auto kfn = address_tc_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)L.total);
+  if (e != cudaSuccess) return e;
+  const long long BT = (long long)A.d.B * A.d.T;
+  const int per = MODE == kAddrScoresOnly ? kTcRows : kTcRows / 2;
+  const long long tiles = (BT + per - 1) / per;
+  if (tiles == 0 || A.d.H == 0) return cudaSuccess;
+  dim3 grid((unsigned)tiles, (unsigned)A.d.H);
+  kfn<<<grid, kTcThreads, L.total, stream>>>(A);
+  return cudaGetLastError();
+}
+
 template <int MODE>
 cudaError_t launch_mode(const AddrArgs& A, cudaStream_t stream) {
+  if (tc_eligible(A.d)) return launch_tc<MODE>(A, stream);
   const bool bf = A.d.in_dtype == SDM_BF16;
   if (A.d.score == SDM_SCORE_DOT)
     return bf ? launch_t<MODE, true, SDM_SCORE_DOT>(A, stream)

@@ -60,11 +60,11 @@ struct MetaSlot {
   uint32_t src_w[64];     // shared-memory byte offset of the row's chunk 0 | flags
   uint32_t src_r[64];
   int16_t code[128];      // plan codes: W write rows then R read rows
-  unsigned char vraw[128];
+  unsigned char vraw[256];
   float alpha, beta, pad0, pad1;
   unsigned char pad[112];
 };
-static_assert(sizeof(MetaSlot) == 2048, "meta slot size");
+static_assert(sizeof(MetaSlot) == 2176, "meta slot size");
 
 struct ScanArgs {
   Dims d;
@@ -576,6 +576,7 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   }
   ScanArgs A{d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, codes, M, y, D, status};
   const bool bf = d.in_dtype == SDM_BF16;
+  if (cw == 64) return bf ? launch_t<64, true>(A, stream) : launch_t<64, false>(A, stream);
   if (cw == 32) return bf ? launch_t<32, true>(A, stream) : launch_t<32, false>(A, stream);
   return bf ? launch_t<16, true>(A, stream) : launch_t<16, false>(A, stream);
 }

@@ -260,7 +260,8 @@ sdm_status sdm_get_device_status(void* stream) {
 
 sdm_status sdm_set_scan_tuning(int depth, int col_slice) {
   if (depth < 0 || depth > 16) return SDM_ERR_INVALID_ARG;
-  if (col_slice != 0 && col_slice != 16 && col_slice != 32) return SDM_ERR_INVALID_ARG;
+  if (col_slice != 0 && col_slice != 16 && col_slice != 32 && col_slice != 64)
+    return SDM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_depth = depth;
   g_colslice = col_slice;

@@ -196,9 +196,9 @@ def oracle_scan(B, H, T, s, dv, W, R, case):
     (1, 1, 64, 4, 16, 16, 16, False),      # W = N
     (1, 2, 77, 8, 48, 1, 1, False),        # d_v not a multiple of 32
 ])
-@pytest.mark.parametrize("depth,cs", [(1, 16), (2, 32), (4, 0), (8, 16), (16, 0)])
+@pytest.mark.parametrize("depth,cs", [(1, 16), (2, 32), (4, 0), (8, 16), (16, 0), (3, 64)])
 def test_scan_matches_oracle(B, H, T, s, dv, W, R, bf16, depth, cs):
-    if cs == 32 and dv % 32:
+    if cs and dv % cs:
         cs = 16
     rng = np.random.default_rng(B * 1000 + T + W)
     case = random_scan_case(rng, B, H, T, s, dv, W, R, bf16)

@@ -38,7 +38,8 @@ namespace sdm {
 namespace {
 
 constexpr int kConsumers = 256;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kLoaders = 128;    // loader threads (4 warps) that fetch the rows
+constexpr int kThreads = kConsumers + 32 + kLoaders;
 constexpr int kP = 4;            // producer's metadata prefetch distance (steps)
 constexpr int kSlack = 4;        // steps the producer may prepare beyond the need
 constexpr uint32_t kFwd = 1u << 30;   // src flag: forwarded, do not fetch
@@ -96,34 +97,13 @@ __host__ __device__ inline ScanLayout scan_layout(int CW, int W, int R, int D) {
   L.wtile = o; o += sizeof(float) * (size_t)L.NS * W * CW;
   L.rtile = o; o += sizeof(float) * (size_t)D * R * CW;
   L.ypart = o; o += sizeof(float) * 2 * 8 * CW;
-  L.bars = o;  o += sizeof(uint64_t) * 2 * L.MR;
+  L.bars = o;  o += sizeof(uint64_t) * (2 * L.MR + D);
   L.total = o;
   return L;
 }
 
 // Codes per token: W + R rounded up to 8 (16-byte rows).
 __host__ __device__ inline int code_pitch(int W, int R) { return (W + R + 7) & ~7; }
-
-__device__ __forceinline__ void cp_async_wait_dyn(int n) {
-  switch (n) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    case 3: cp_async_wait<3>(); break;
-    case 4: cp_async_wait<4>(); break;
-    case 5: cp_async_wait<5>(); break;
-    case 6: cp_async_wait<6>(); break;
-    case 7: cp_async_wait<7>(); break;
-    case 8: cp_async_wait<8>(); break;
-    case 9: cp_async_wait<9>(); break;
-    case 10: cp_async_wait<10>(); break;
-    case 11: cp_async_wait<11>(); break;
-    case 12: cp_async_wait<12>(); break;
-    case 13: cp_async_wait<13>(); break;
-    case 14: cp_async_wait<14>(); break;
-    default: cp_async_wait<15>(); break;
-  }
-}
 
 template <bool BF16>
 __device__ __forceinline__ float4 load_v4(const unsigned char* vraw, int c) {
@@ -229,7 +209,7 @@ struct Ring {
 };
 
 template <int CW, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1) scan_kernel(const ScanArgs A) {
+__global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
   constexpr int CH = CW / 4;               // 16-byte chunks per row slice
   constexpr int RP = kConsumers / CH;      // rows per consumer pass
   constexpr int IB = BF16 ? 2 : 4;         // input element bytes
@@ -251,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const ScanArgs A) {
   float* ypart = reinterpret_cast<float*>(smem + L.ypart);
   uint64_t* mfull = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* mempty = mfull + MR;
+  uint64_t* rfull = mempty + MR;     // rows of step u landed (ring of D)
   const uint32_t wslot = (uint32_t)(W * CW * 4), rslot = (uint32_t)(R * CW * 4);
   constexpr uint32_t rowb = (uint32_t)(CW * 4);
 
@@ -260,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const ScanArgs A) {
       mbar_init(&mfull[i], 32);
       mbar_init(&mempty[i], kConsumers / 32);
     }
+    for (int i = 0; i < D; ++i) mbar_init(&rfull[i], kLoaders);
   }
   __syncthreads();
 
@@ -376,6 +358,44 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const ScanArgs A) {
     return;
   }
 
+  if (warp > kConsumers / 32) {
+    // -------------------------------------------------------------- loaders
+    // Fetch the rows of step u once its metadata is decoded and the
+    // consumers have finished step u - D (whose writes it must see, and whose
+    // read tile it reuses).  Completion is signalled on rfull[u % D].
+    const int lt = tid - (kConsumers + 32);
+    const int lc = lt % CH, lr = lt / CH;
+    constexpr int LRP = kLoaders / CH;       // rows per loader pass
+    float* Ml = Mc + 4 * lc;
+    unsigned char* sm_l = smem + 16 * lc;
+    Ring mu{0, MR, 0u}, me{0, MR, 0u}, rf{0, D, 0u};
+    bool ok = true;
+    for (int u = 0; u < T && ok; ++u) {
+      if (lane == 0) {
+        ok = mbar_wait_bounded(&mfull[mu.i], mu.phase, kTimeoutNs);
+        if (ok && u >= D) ok = mbar_wait_bounded(&mempty[me.i], me.phase, kTimeoutNs);
+      }
+      __syncwarp();
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);
+        break;
+      }
+      const MetaSlot* m = meta + mu.i;
+      for (int k = lr; k < W + R; k += LRP) {
+        const uint32_t sv = k < W ? m->src_w[k] : m->src_r[k - W];
+        const int row = k < W ? m->idx_w[k] : m->idx_r[k - W];
+        if (!(sv & (kFwd | kSkip))) cp_async16(sm_l + (sv & kOffMask), Ml + (size_t)row * dv);
+      }
+      cp_async_mbar_arrive_noinc(&rfull[rf.i]);
+      mu.next();
+      if (u >= D) me.next();
+      rf.next();
+    }
+    cp_async_wait_all();
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   const int myc = tid % CH, myr = tid / CH;
   const int PW = (W + RP - 1) / RP, PR = (R + RP - 1) / RP;
@@ -383,32 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const ScanArgs A) {
   unsigned char* sm_c = smem + 16 * myc;     // shared base shifted to the chunk
   bool aborted = false;
 
-  auto wait_meta = [&](const Ring& r) {
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait_bounded(&mfull[r.i], r.phase, kTimeoutNs);
-    __syncwarp();
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) {
-      if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);
-      aborted = true;
-    }
-  };
-  auto issue = [&](const MetaSlot* m) {
-    for (int pw = 0; pw < PW; ++pw) {
-      const int j = pw * RP + myr;
-      if (j >= W) break;
-      const uint32_t s = m->src_w[j];
-      const int row = m->idx_w[j];
-      if (!(s & (kFwd | kSkip))) cp_async16(sm_c + (s & kOffMask), Mt + (size_t)row * dv);
-    }
-    for (int pr = 0; pr < PR; ++pr) {
-      const int q = pr * RP + myr;
-      if (q >= R) break;
-      const uint32_t s = m->src_r[q];
-      const int row = m->idx_r[q];
-      if (!(s & (kFwd | kSkip))) cp_async16(sm_c + (s & kOffMask), Mt + (size_t)row * dv);
-    }
-  };
   auto finalize = [&](int t) {
     if (lane < CH) {
       const float* yp = ypart + (t & 1) * 8 * CW + 4 * lane;
@@ -426,19 +420,22 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const ScanArgs A) {
   };
 
   Ring mt{0, MR, 0u};   // metadata slot of step t
-  Ring mu{0, MR, 0u};   // metadata slot of step t + D (next to fetch)
   Ring wt{0, NS, 0u};   // write-tile slot of step t
-  for (int u = 0; u < D; ++u) {
-    if (u < T && !aborted) {
-      wait_meta(mu);
-      if (!aborted) issue(meta + mu.i);
-    }
-    if (u < T) mu.next();
-    cp_async_commit();
-  }
+  Ring rf{0, D, 0u};    // rows-landed barrier of step t
 
   for (int t = 0; t < T; ++t) {
-    cp_async_wait_dyn(D - 1);
+    if (!aborted) {
+      // Rows of step t landed (and its metadata is decoded).
+      bool ok = true;
+      if (lane == 0)
+        ok = mbar_wait_bounded(&rfull[rf.i], rf.phase, kTimeoutNs) &&
+             mbar_wait_bounded(&mfull[mt.i], mt.phase, kTimeoutNs);
+      __syncwarp();
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);
+        aborted = true;
+      }
+    }
     const MetaSlot* m = meta + mt.i;
     if (!aborted) {
       // Write: decay + per-slot delta (Eq. (3)-(4)).
@@ -499,20 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const ScanArgs A) {
     if (lane < CH) *reinterpret_cast<float4*>(ypart + (t & 1) * 8 * CW + warp * CW + 4 * lane) = acc;
     __syncwarp();
     if (lane == 0) mbar_arrive(&mempty[mt.i]);
-    if (t + D < T) {
-      if (!aborted) {
-        wait_meta(mu);
-        if (!aborted) issue(meta + mu.i);
-      }
-      mu.next();
-    }
-    cp_async_commit();
     mt.next();
     wt.next();
+    rf.next();
   }
   named_bar_sync(1, kConsumers);
   if (!aborted && T > 0 && warp == ((T - 1) & 7)) finalize(T - 1);
-  cp_async_wait_all();
 }
 
 template <int CW, bool BF16>

@@ -72,7 +72,7 @@ typedef struct {
 
 /* Limits (anything else returns SDM_ERR_UNSUPPORTED):
  *   1 <= n_sub <= 512;  d_h in {16, 32, 64, 128, 256};  d_v a multiple of 16,
- *   16 <= d_v <= 1024;  1 <= W, R <= 64;  1 <= k <= min(64, n_sub) and
+ *   16 <= d_v <= 2048;  1 <= W, R <= 64;  1 <= k <= min(64, n_sub) and
  *   W <= k_w^2, R <= k_r^2;  B*H*N*d_v < 2^40 elements;  B, H, T >= 0. */
 
 /* Human-readable name of a status code (static string). */
@@ -121,6 +121,8 @@ size_t sdm_workspace_size(const sdm_shape* shape);
  *   y: [B,H,T,d_v] float32 out;
  *   workspace: device scratch of at least sdm_workspace_size(shape) bytes
  *   (ws_bytes), caller-owned, contents irrelevant on entry and on return.
+ * shape->update selects the write: Eq. (4) per slot, or the shared residual
+ * read off Fig. 2 (one prediction sum_j w_j M~[j] for the whole write set).
  * Write slots of one step must be distinct and all slots in [0, N); the
  * device checks both, skips the offending rows and records
  * SDM_ERR_DUPLICATE_SLOT / SDM_ERR_DEVICE_BOUNDS.  Calling this on

@@ -5,6 +5,12 @@
 // M[i] = M~[i] + beta_t w_i (v_t - M~[i]); other rows are untouched; then
 // y_t = sum_{i in read set} q_i M_t[i] reads the table after the write.
 //
+// The Fig. 2 reading of the write ([SDM notes] 2.5) is the second update
+// form: the decayed rows' weighted sum vhat = sum_j w_j M~[j] is one
+// prediction shared by the write set, M[i] = M~[i] + beta_t w_i (v_t - vhat).
+// It needs the whole write set before any row is written: one more block
+// reduction per step.
+//
 // Parallel units: (chain = (b,h), column slice of CW floats).  The update
 // acts column by column with per-row scalars, so slices of one chain never
 // communicate, and a step's write slots are distinct, so no atomics.
@@ -84,7 +90,7 @@ struct ScanArgs {
 };
 
 struct ScanLayout {
-  size_t meta, wtile, rtile, ypart, bars, total;
+  size_t meta, wtile, rtile, ypart, vpart, bars, total;
   int NS, MR;
 };
 
@@ -97,6 +103,7 @@ __host__ __device__ inline ScanLayout scan_layout(int CW, int W, int R, int D) {
   L.wtile = o; o += sizeof(float) * (size_t)L.NS * W * CW;
   L.rtile = o; o += sizeof(float) * (size_t)D * R * CW;
   L.ypart = o; o += sizeof(float) * 2 * 8 * CW;
+  L.vpart = o; o += sizeof(float) * 8 * CW;      // per-warp partials of vhat (Fig. 2 form)
   L.bars = o;  o += sizeof(uint64_t) * (2 * L.MR + D);
   L.total = o;
   return L;
@@ -208,7 +215,7 @@ struct Ring {
   }
 };
 
-template <int CW, bool BF16>
+template <int CW, bool BF16, bool FIG2>
 __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
   constexpr int CH = CW / 4;               // 16-byte chunks per row slice
   constexpr int RP = kConsumers / CH;      // rows per consumer pass
@@ -229,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
 
   MetaSlot* meta = reinterpret_cast<MetaSlot*>(smem + L.meta);
   float* ypart = reinterpret_cast<float*>(smem + L.ypart);
+  float* vpart = reinterpret_cast<float*>(smem + L.vpart);
   uint64_t* mfull = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* mempty = mfull + MR;
   uint64_t* rfull = mempty + MR;     // rows of step u landed (ring of D)
@@ -437,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
       }
     }
     const MetaSlot* m = meta + mt.i;
-    if (!aborted) {
+    if (!FIG2 && !aborted) {
       // Write: decay + per-slot delta (Eq. (3)-(4)).
       const float a = m->alpha, b = m->beta;
       const float4 vv = load_v4<BF16>(m->vraw, myc);
@@ -460,6 +468,74 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
         mt_ = a * x.y; o.y = fmaf(cw, vv.y - mt_, mt_);
         mt_ = a * x.z; o.z = fmaf(cw, vv.z - mt_, mt_);
         mt_ = a * x.w; o.w = fmaf(cw, vv.w - mt_, mt_);
+        *reinterpret_cast<float4*>(wdst + j * rowb) = o;
+        *reinterpret_cast<float4*>(Mt + (size_t)row * dv) = o;
+      }
+    }
+    if (FIG2) {
+      // Write, Fig. 2 form: decay every write row, reduce the shared
+      // prediction vhat over the write set, then one residual for all rows.
+      constexpr int kMaxPW = (64 + RP - 1) / RP;
+      float4 md[kMaxPW];
+      const float a = m->alpha;
+      unsigned char* wdst = sm_c + L.wtile + wt.i * wslot;
+      float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!aborted) {
+#pragma unroll
+        for (int pw = 0; pw < kMaxPW; ++pw) {
+          const int j = pw * RP + myr;
+          md[pw] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (j >= W) continue;
+          const uint32_t s = m->src_w[j];
+          if (s & kSkip) continue;
+          const float4 x = *reinterpret_cast<const float4*>(
+              (s & kFwd) ? sm_c + (s & kOffMask) : wdst + j * rowb);
+          const float wj = m->wt_w[j];
+          md[pw] = make_float4(a * x.x, a * x.y, a * x.z, a * x.w);
+          part.x = fmaf(wj, md[pw].x, part.x);
+          part.y = fmaf(wj, md[pw].y, part.y);
+          part.z = fmaf(wj, md[pw].z, part.z);
+          part.w = fmaf(wj, md[pw].w, part.w);
+        }
+#pragma unroll
+        for (int off = CH; off < 32; off <<= 1) {
+          part.x += __shfl_xor_sync(0xffffffffu, part.x, off);
+          part.y += __shfl_xor_sync(0xffffffffu, part.y, off);
+          part.z += __shfl_xor_sync(0xffffffffu, part.z, off);
+          part.w += __shfl_xor_sync(0xffffffffu, part.w, off);
+        }
+        if (lane < CH) *reinterpret_cast<float4*>(vpart + warp * CW + 4 * lane) = part;
+      }
+      // Every consumer reaches this barrier each step (a timeout becomes a
+      // uniform exit here, as at the step barrier below).
+      if (named_bar_or(2, kConsumers, aborted)) {
+        aborted = true;
+        break;
+      }
+      const float b = m->beta;
+      const float4 vv = load_v4<BF16>(m->vraw, myc);
+      float4 vh = *reinterpret_cast<const float4*>(vpart + 4 * myc);
+#pragma unroll
+      for (int w = 1; w < 8; ++w) {
+        const float4 p = *reinterpret_cast<const float4*>(vpart + w * CW + 4 * myc);
+        vh.x += p.x;
+        vh.y += p.y;
+        vh.z += p.z;
+        vh.w += p.w;
+      }
+      const float4 res = make_float4(vv.x - vh.x, vv.y - vh.y, vv.z - vh.z, vv.w - vh.w);
+#pragma unroll
+      for (int pw = 0; pw < kMaxPW; ++pw) {
+        const int j = pw * RP + myr;
+        if (j >= W) continue;
+        if (m->src_w[j] & kSkip) continue;
+        const int row = m->idx_w[j];
+        const float cw = b * m->wt_w[j];
+        float4 o;
+        o.x = fmaf(cw, res.x, md[pw].x);
+        o.y = fmaf(cw, res.y, md[pw].y);
+        o.z = fmaf(cw, res.z, md[pw].z);
+        o.w = fmaf(cw, res.w, md[pw].w);
         *reinterpret_cast<float4*>(wdst + j * rowb) = o;
         *reinterpret_cast<float4*>(Mt + (size_t)row * dv) = o;
       }
@@ -507,7 +583,8 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
 template <int CW, bool BF16>
 cudaError_t launch_t(const ScanArgs& A, cudaStream_t stream) {
   const size_t smem = scan_layout(CW, A.d.W, A.d.R, A.depth).total;
-  auto kfn = scan_kernel<CW, BF16>;
+  auto kfn = A.d.update == SDM_UPDATE_SHARED_RESIDUAL ? scan_kernel<CW, BF16, true>
+                                                      : scan_kernel<CW, BF16, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

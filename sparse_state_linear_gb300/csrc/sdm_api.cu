@@ -56,9 +56,8 @@ sdm_status check_shape(const sdm_shape* sh, Dims* d) {
   if (s > 512) return SDM_ERR_UNSUPPORTED;
   if (sh->d_h != 16 && sh->d_h != 32 && sh->d_h != 64 && sh->d_h != 128 && sh->d_h != 256)
     return SDM_ERR_UNSUPPORTED;
-  if (sh->d_v % 16 != 0 || sh->d_v > 1024) return SDM_ERR_UNSUPPORTED;
+  if (sh->d_v % 16 != 0 || sh->d_v > 2048) return SDM_ERR_UNSUPPORTED;
   if (sh->W > 64 || sh->R > 64 || kw > 64 || kr > 64) return SDM_ERR_UNSUPPORTED;
-  if (sh->update != SDM_UPDATE_EQ4) return SDM_ERR_UNSUPPORTED;
   const long long N = (long long)s * s;
   if ((long long)sh->B * sh->H * N * sh->d_v >= (1ll << 40)) return SDM_ERR_UNSUPPORTED;
   if ((long long)sh->B * sh->H * sh->T >= (1ll << 31)) return SDM_ERR_UNSUPPORTED;

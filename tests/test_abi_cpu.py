@@ -60,7 +60,7 @@ def scan_rc(L, sh, ptrs=None, ws_bytes=1 << 30):
     (dict(W=300), 1),                    # W > k_w^2 with k_w = min(W, s) = 16
     (dict(k_w=17), 1),                   # k above s
     (dict(n_sub=600), 2), (dict(d_h=24), 2), (dict(d_v=40), 2), (dict(n_sub=32, W=65, R=8), 2),
-    (dict(update=1), 2),
+    (dict(d_v=2064), 2),
 ])
 def test_scan_rejects_bad_shapes(L, kw, code):
     assert scan_rc(L, good_shape(**kw)) == code

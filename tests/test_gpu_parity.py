@@ -152,6 +152,59 @@ def test_address_end_to_end(name):
     assert np.max(np.abs(ww[same] - ow[2][same])) < 1e-5
 
 
+ROW_SHAPES = [  # bf16 dot scores: the one-thread-per-row kernel
+    dict(n_sub=32, d_h=16, W=8, R=8, T=90),
+    dict(n_sub=40, d_h=32, W=5, R=3, k_w=12, k_r=2, T=70),    # s % 16 != 0, W % 4 != 0
+    dict(n_sub=200, d_h=64, W=64, R=16, T=130),
+    dict(n_sub=256, d_h=64, W=1, R=64, T=66),
+    dict(n_sub=16, d_h=16, W=64, R=64, T=65),                 # k = s = 16
+    dict(n_sub=64, d_h=32, W=36, R=64, T=129),
+]
+
+
+def address_checks(w, x, sh_g, sh_o, iw, ww, ir, wr, g):
+    """Bit-exact against the oracle's selection on the device's own sub-scores,
+    and weights against the oracle's softmax of those selections."""
+    Sg_w = np32(sdm.sdm_subscores(sh_g, g["q_w"], g["K"]))
+    Sg_r = np32(sdm.sdm_subscores(sh_g, g["q_r"], g["K"]))
+    ow, orr = O.select(sh_o, 0, Sg_w), O.select(sh_o, 1, Sg_r)
+    assert np.array_equal(iw, ow[0])
+    assert np.array_equal(ir, orr[0])
+    assert np.max(np.abs(ww - ow[2])) < 1e-5
+    assert np.max(np.abs(wr - orr[2])) < 1e-5
+
+
+@pytest.mark.parametrize("ov", ROW_SHAPES, ids=lambda o: "s{n_sub}_W{W}_R{R}".format(**o))
+def test_address_row_kernel_shapes(ov):
+    w = WORKLOADS["mid"].with_(B=2, H=2, **ov)
+    x = generate(w)
+    sh_g, sh_o = gshape(w, sdm), oshape(w)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    iw, ww, ir, wr = sdm.sdm_address(sh_g, g["q_w"], g["q_r"], g["K"])
+    status_ok()
+    address_checks(w, x, sh_g, sh_o, *(t.cpu().numpy() for t in (iw, ww, ir, wr)), g)
+
+
+def test_address_degenerate_rows_take_exact_path():
+    """Rows the per-row kernel leaves to the exact warp kernel: all-zero
+    queries (every score equal), one constant half (equal sums along a row of
+    the staircase), duplicated sub-keys (equal scores inside a half)."""
+    w = WORKLOADS["gdn_matched"].with_(B=1, H=2, T=200)
+    x = generate(w)
+    x["q_w"][0, 0, 3:40] = 0
+    x["q_r"][0, 1, 10:30, 0] = 0
+    x["q_w"][0, 1, 50:70, 1] = 0
+    x["K"][0, 0, 100:140] = x["K"][0, 0, 20]
+    x["K"][1, 1, 7:9] = x["K"][1, 1, 3]
+    sh_g, sh_o = gshape(w, sdm), oshape(w)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    iw, ww, ir, wr = sdm.sdm_address(sh_g, g["q_w"], g["q_r"], g["K"])
+    status_ok()
+    iw, ww, ir, wr = (t.cpu().numpy() for t in (iw, ww, ir, wr))
+    assert (iw >= 0).all() and (ir >= 0).all()
+    address_checks(w, x, sh_g, sh_o, iw, ww, ir, wr, g)
+
+
 # ------------------------------------------------------------------ scan
 
 def random_scan_case(rng, B, H, T, s, dv, W, R, bf16):
@@ -181,9 +234,9 @@ def run_scan(sh_g, case, depth=0, cs=0):
     return M.cpu().numpy(), y.cpu().numpy()
 
 
-def oracle_scan(B, H, T, s, dv, W, R, case):
+def oracle_scan(B, H, T, s, dv, W, R, case, update_form=0):
     idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0 = case
-    sh = O.Shape(B=B, H=H, T=T, n_sub=s, d_h=16, d_v=dv, W=W, R=R)
+    sh = O.Shape(B=B, H=H, T=T, n_sub=s, d_h=16, d_v=dv, W=W, R=R, update_form=update_form)
     return O.scan(sh, idx_w, wt_w.astype(np.float64), idx_r, wt_r.astype(np.float64),
                   np32(alpha), np32(beta), np32(v), M0)
 
@@ -215,6 +268,47 @@ def test_scan_matches_oracle(B, H, T, s, dv, W, R, bf16, depth, cs):
             untouched = np.ones(s * s, bool)
             untouched[idx_w[b, h].ravel()] = False
             assert np.array_equal(Mg[b, h, untouched], M0[b, h, untouched])
+
+
+@pytest.mark.parametrize("B,H,T,s,dv,W,R,bf16", [
+    (1, 1, 200, 8, 32, 16, 16, False),     # consecutive steps collide constantly
+    (2, 3, 150, 16, 64, 32, 48, True),
+    (1, 2, 120, 32, 128, 64, 64, True),
+    (1, 1, 64, 4, 16, 16, 16, False),      # W = N: the write set is the whole table
+    (1, 2, 77, 8, 48, 1, 1, False),
+    (1, 1, 40, 16, 1920, 64, 64, True),    # the 8B-scale value width
+])
+@pytest.mark.parametrize("depth,cs", [(1, 16), (4, 32), (8, 64), (0, 0)])
+def test_scan_fig2_matches_oracle(B, H, T, s, dv, W, R, bf16, depth, cs):
+    """The shared-residual write read off Fig. 2, against the oracle's form 1."""
+    if cs and dv % cs:
+        cs = 16
+    rng = np.random.default_rng(B * 7000 + T + W)
+    case = random_scan_case(rng, B, H, T, s, dv, W, R, bf16)
+    sh_g = sdm.make_shape(B, H, T, s, 16, dv, W, R,
+                          in_dtype=sdm.SDM_BF16 if bf16 else sdm.SDM_F32,
+                          update=sdm.SDM_UPDATE_SHARED_RESIDUAL)
+    Mg, yg = run_scan(sh_g, case, depth, cs)
+    Mo, yo = oracle_scan(B, H, T, s, dv, W, R, case, update_form=1)
+    assert max_rel(yg, yo) <= FTOL
+    assert max_rel(Mg, Mo) <= FTOL
+    idx_w, M0 = case[0], case[-1]
+    for b in range(B):
+        for h in range(H):
+            untouched = np.ones(s * s, bool)
+            untouched[idx_w[b, h].ravel()] = False
+            assert np.array_equal(Mg[b, h, untouched], M0[b, h, untouched])
+
+
+def test_scan_fig2_differs_from_eq4():
+    """The two forms are different maps: the same inputs give different tables."""
+    rng = np.random.default_rng(5)
+    B, H, T, s, dv, W, R = 1, 1, 50, 16, 32, 8, 8
+    case = random_scan_case(rng, B, H, T, s, dv, W, R, False)
+    M4, _ = run_scan(sdm.make_shape(B, H, T, s, 16, dv, W, R, in_dtype=sdm.SDM_F32), case)
+    M2, _ = run_scan(sdm.make_shape(B, H, T, s, 16, dv, W, R, in_dtype=sdm.SDM_F32,
+                                    update=sdm.SDM_UPDATE_SHARED_RESIDUAL), case)
+    assert max_rel(M4, M2) > 1e-3
 
 
 def test_scan_depth_invariance_bitwise():
@@ -249,7 +343,15 @@ def test_scan_segments_equal_one_call():
 
 @pytest.mark.parametrize("name", list(REDUCED))
 def test_forward_end_to_end(name):
-    w = WORKLOADS[name].with_(**REDUCED[name])
+    forward_check(WORKLOADS[name].with_(**REDUCED[name]))
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid", "gdn_matched"])
+def test_forward_fig2_end_to_end(name):
+    forward_check(WORKLOADS[name].with_(update_form=1, **REDUCED[name]))
+
+
+def forward_check(w):
     x = generate(w)
     sh_g, sh_o = gshape(w, sdm), oshape(w)
     g = {k: t.to(DEV) for k, t in x.items()}

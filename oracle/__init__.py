@@ -84,8 +84,10 @@ def _L():
         _lib.sdm_ref_select.argtypes = [sp, ctypes.c_int, P, P, P, P]
         _lib.sdm_ref_scan.argtypes = [sp] + [P] * 9
         _lib.sdm_ref_forward.argtypes = [sp] + [P] * 12
+        _lib.sdm_ref_scan_logged.argtypes = [sp] + [P] * 10
+        _lib.sdm_ref_undo.argtypes = [sp] + [P] * 3
         for f in (_lib.sdm_ref_subscores, _lib.sdm_ref_select, _lib.sdm_ref_scan,
-                  _lib.sdm_ref_forward):
+                  _lib.sdm_ref_forward, _lib.sdm_ref_scan_logged, _lib.sdm_ref_undo):
             f.restype = ctypes.c_int
     return _lib
 
@@ -130,8 +132,10 @@ def select(sh: Shape, which: int, S):
     return idx, sc, wt
 
 
-def scan(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0):
-    """Returns (M float64 [B,H,N,d_v], y float64 [B,H,T,d_v]); M0 is not modified."""
+def scan(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0, log: bool = False):
+    """Returns (M float64 [B,H,N,d_v], y float64 [B,H,T,d_v]); M0 is not modified.
+    With log=True also the undo log float64 [B,H,T,W,d_v]: the value each
+    written row had just before its step's write."""
     idx_w = _arr(idx_w, np.int32)
     idx_r = _arr(idx_r, np.int32)
     wt_w = _arr(wt_w, np.float64)
@@ -147,9 +151,29 @@ def scan(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0):
     assert M.shape == (sh.B, sh.H, sh.N, sh.d_v)
     y = np.empty((sh.B, sh.H, sh.T, sh.d_v), np.float64)
     cs = sh.c()
+    if log:
+        U = np.empty((sh.B, sh.H, sh.T, sh.W, sh.d_v), np.float64)
+        _check(_L().sdm_ref_scan_logged(ctypes.byref(cs), _p(idx_w), _p(wt_w), _p(idx_r),
+                                        _p(wt_r), _p(alpha), _p(beta), _p(v), _p(M), _p(y),
+                                        _p(U)), "scan_logged")
+        return M, y, U
     _check(_L().sdm_ref_scan(ctypes.byref(cs), _p(idx_w), _p(wt_w), _p(idx_r), _p(wt_r),
                              _p(alpha), _p(beta), _p(v), _p(M), _p(y)), "scan")
     return M, y
+
+
+def undo(sh: Shape, idx_w, U, M1):
+    """Restore the table before a logged segment: M1 [B,H,N,d_v] after it,
+    U its undo log [B,H,T,W,d_v]; returns the restored float64 table."""
+    idx_w = _arr(idx_w, np.int32)
+    U = _arr(U, np.float64)
+    M = np.array(M1, dtype=np.float64, order="C", copy=True)
+    assert idx_w.shape == (sh.B, sh.H, sh.T, sh.W)
+    assert U.shape == (sh.B, sh.H, sh.T, sh.W, sh.d_v)
+    assert M.shape == (sh.B, sh.H, sh.N, sh.d_v)
+    cs = sh.c()
+    _check(_L().sdm_ref_undo(ctypes.byref(cs), _p(idx_w), _p(U), _p(M)), "undo")
+    return M
 
 
 def forward(sh: Shape, q_w, q_r, K, alpha, beta, v, M0):

@@ -141,11 +141,15 @@ extern "C" int sdm_ref_select(const sdm_ref_shape* sh, int which, const float* S
 // Eq. (5): y_t = sum_{i in read set} q^(i) M_t[i], read after the write.
 // update_form 1 ([SDM notes] 2.5, reading of Fig. 2): the residual is shared,
 //   vhat = sum_j k^(j) M~[j];  M[i] = M~[i] + beta_t k^(i) (v_t - vhat).
-extern "C" int sdm_ref_scan(const sdm_ref_shape* sh, const int32_t* idx_w,
-                            const double* wt_w, const int32_t* idx_r,
-                            const double* wt_r, const float* alpha,
-                            const float* beta, const float* v, double* M,
-                            double* y) {
+// When `undo` is given, the value every written row had just before the
+// write of step t is copied to undo[b,h,t,j,:] ([SDM notes] 2.9, appendix
+// A.3 "backward memory": the forward pass writes in place and the backward
+// pass restores earlier states by undoing the sparse writes, for O(T W d_v)
+// extra memory -- i.e. a log of the W overwritten rows of every step).
+static int scan_impl(const sdm_ref_shape* sh, const int32_t* idx_w, const double* wt_w,
+                     const int32_t* idx_r, const double* wt_r, const float* alpha,
+                     const float* beta, const float* v, double* M, double* y,
+                     double* undo) {
   if (!shape_ok(sh) || !idx_w || !wt_w || !idx_r || !wt_r || !alpha || !beta ||
       !v || !M || !y)
     return -1;
@@ -170,6 +174,13 @@ extern "C" int sdm_ref_scan(const sdm_ref_shape* sh, const int32_t* idx_w,
         const size_t row = ((size_t)b * H + h) * T + t;
         const double a = alpha[row], be = beta[row];
         const float* vt = v + row * dv;
+        if (undo) {
+          for (int j = 0; j < W; ++j) {
+            const double* m = Mc + (size_t)idx_w[row * W + j] * dv;
+            double* u = undo + (row * W + j) * (size_t)dv;
+            for (int col = 0; col < dv; ++col) u[col] = m[col];
+          }
+        }
         if (sh->update_form == 0) {
           for (int j = 0; j < W; ++j) {
             double* m = Mc + (size_t)idx_w[row * W + j] * dv;
@@ -200,6 +211,48 @@ extern "C" int sdm_ref_scan(const sdm_ref_shape* sh, const int32_t* idx_w,
           const double* m = Mc + (size_t)idx_r[row * R + j] * dv;
           const double q = wt_r[row * R + j];
           for (int col = 0; col < dv; ++col) yt[col] += q * m[col];
+        }
+      }
+    }
+  return 0;
+}
+
+extern "C" int sdm_ref_scan(const sdm_ref_shape* sh, const int32_t* idx_w,
+                            const double* wt_w, const int32_t* idx_r,
+                            const double* wt_r, const float* alpha,
+                            const float* beta, const float* v, double* M,
+                            double* y) {
+  return scan_impl(sh, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, nullptr);
+}
+
+extern "C" int sdm_ref_scan_logged(const sdm_ref_shape* sh, const int32_t* idx_w,
+                                   const double* wt_w, const int32_t* idx_r,
+                                   const double* wt_r, const float* alpha,
+                                   const float* beta, const float* v, double* M,
+                                   double* y, double* undo) {
+  if (!undo) return -1;
+  return scan_impl(sh, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, undo);
+}
+
+// Undo a segment ([SDM notes] 2.9, A.3): walk the steps backwards and put
+// every logged row back; a row written at several steps ends with the copy
+// of its earliest write, i.e. the value it had before the segment.
+extern "C" int sdm_ref_undo(const sdm_ref_shape* sh, const int32_t* idx_w,
+                            const double* undo, double* M) {
+  if (!shape_ok(sh) || !idx_w || !undo || !M) return -1;
+  const int B = sh->B, H = sh->H, T = sh->T, W = sh->W, dv = sh->d_v;
+  const long long N = (long long)sh->n_sub * sh->n_sub;
+  for (size_t i = 0; i < (size_t)B * H * T * W; ++i)
+    if (idx_w[i] < 0 || idx_w[i] >= N) return -2;
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h) {
+      double* Mc = M + ((size_t)b * H + h) * (size_t)N * dv;
+      for (int t = T - 1; t >= 0; --t) {
+        const size_t row = ((size_t)b * H + h) * T + t;
+        for (int j = 0; j < W; ++j) {
+          double* m = Mc + (size_t)idx_w[row * W + j] * dv;
+          const double* u = undo + (row * W + j) * (size_t)dv;
+          for (int col = 0; col < dv; ++col) m[col] = u[col];
         }
       }
     }

@@ -67,6 +67,20 @@ int sdm_ref_scan(const sdm_ref_shape* sh,
                  const float* alpha, const float* beta, const float* v,
                  double* M, double* y);
 
+/* sdm_ref_scan that also logs, before each step's write, the value of every
+ * row it writes: undo [B,H,T,W,d_v] out (double), undo[b,h,t,j,:] =
+ * M_{t-1}[idx_w[b,h,t,j], :]. */
+int sdm_ref_scan_logged(const sdm_ref_shape* sh,
+                        const int32_t* idx_w, const double* wt_w,
+                        const int32_t* idx_r, const double* wt_r,
+                        const float* alpha, const float* beta, const float* v,
+                        double* M, double* y, double* undo);
+
+/* Restore M [B,H,N,d_v] (in/out, double) to its value before a logged
+ * segment: steps T-1 down to 0 put their logged rows back. */
+int sdm_ref_undo(const sdm_ref_shape* sh, const int32_t* idx_w,
+                 const double* undo, double* M);
+
 /* Sub-scores, both selections and the scan, in that order.  The selected
  * indices and weights are returned too (none of the idx and wt outputs may be NULL). */
 int sdm_ref_forward(const sdm_ref_shape* sh,

@@ -352,3 +352,73 @@ def test_scan_rejects_bad_indices(oracle_mod):
         O.scan(shape, np.array([0, 4], np.int32).reshape(1, 1, 1, 2), **args)
     with pytest.raises(ValueError):
         O.scan(shape, np.array([1, 1], np.int32).reshape(1, 1, 1, 2), **args)
+
+
+# ------------------------------------------------------------------ undo log
+# [SDM notes] 2.9 (appendix A.3, backward memory): the forward pass writes in
+# place; earlier states come back by undoing the sparse writes, for O(T W d_v)
+# memory -- a log of the rows each step overwrote.
+
+def test_logged_scan_equals_plain_scan(oracle_mod):
+    rng = np.random.default_rng(21)
+    shape = sh(B=2, H=2, T=25, n_sub=4, d_v=5, W=6, R=3)     # N=16: heavy reuse
+    args = random_scan_inputs(rng, shape)
+    M, y = O.scan(shape, *args)
+    M2, y2, U = O.scan(shape, *args, log=True)
+    assert np.array_equal(M, M2) and np.array_equal(y, y2)
+    assert U.shape == (2, 2, 25, 6, 5)
+
+
+@pytest.mark.parametrize("form", [0, 1])
+def test_undo_log_holds_pre_write_rows(oracle_mod, form):
+    """Brute force: the log row of (t, j) is row idx_w[t, j] of the table after
+    the first t steps, computed by an independent scan of those steps."""
+    rng = np.random.default_rng(22 + form)
+    shape = sh(B=1, H=2, T=12, n_sub=3, d_v=4, W=4, R=2, update_form=form)
+    idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0 = random_scan_inputs(rng, shape)
+    _, _, U = O.scan(shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0, log=True)
+    Mt = M0.astype(np.float64)
+    for t in range(shape.T):
+        for h in range(2):
+            for j in range(shape.W):
+                assert np.array_equal(U[0, h, t, j], Mt[0, h, idx_w[0, h, t, j]])
+        one = sh(B=1, H=2, T=1, n_sub=3, d_v=4, W=4, R=2, update_form=form)
+        st = slice(t, t + 1)
+        Mt, _ = O.scan(one, idx_w[:, :, st], wt_w[:, :, st], idx_r[:, :, st], wt_r[:, :, st],
+                       alpha[:, :, st], beta[:, :, st], v[:, :, st], Mt)
+
+
+def test_undo_log_closed_form_single_slot(oracle_mod):
+    """W=1, weight 1, constant gates: the row before step t is
+    m* + (m0 - m*) r^t with r = alpha (1 - beta), m* = beta v / (1 - r)."""
+    T, a, b, v0, m0 = 9, 0.9, 0.3, 2.0, 0.5
+    shape = sh(T=T, n_sub=2, d_v=1, W=1, R=1)
+    ones = np.ones((1, 1, T, 1))
+    idx = np.full((1, 1, T, 1), 3, np.int32)
+    M0 = np.zeros((1, 1, 4, 1)); M0[0, 0, 3, 0] = m0
+    _, _, U = O.scan(shape, idx, ones, idx, ones, np.full((1, 1, T), a, np.float32),
+                     np.full((1, 1, T), b, np.float32), np.full((1, 1, T, 1), v0, np.float32),
+                     M0, log=True)
+    af, bf = float(np.float32(a)), float(np.float32(b))
+    r = af * (1 - bf)
+    ms = bf * v0 / (1 - r)
+    for t in range(T):
+        assert U[0, 0, t, 0, 0] == pytest.approx(ms + (m0 - ms) * r ** t, rel=1e-12)
+
+
+@pytest.mark.parametrize("form", [0, 1])
+def test_undo_restores_the_segment_start(oracle_mod, form):
+    """undo(tail) on the table after prefix+tail gives back exactly the table
+    after the prefix (the earliest logged copy of a reused row wins)."""
+    rng = np.random.default_rng(24 + form)
+    full = sh(B=2, H=1, T=40, n_sub=4, d_v=3, W=5, R=2, update_form=form)
+    idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0 = random_scan_inputs(rng, full)
+    for t0 in (0, 1, 17, 39):
+        pre = sh(B=2, H=1, T=t0, n_sub=4, d_v=3, W=5, R=2, update_form=form)
+        tail = sh(B=2, H=1, T=40 - t0, n_sub=4, d_v=3, W=5, R=2, update_form=form)
+        cut = lambda a, s: a[:, :, s]
+        P = (idx_w, wt_w, idx_r, wt_r, alpha, beta, v)
+        Mp, _ = O.scan(pre, *(cut(a, slice(0, t0)) for a in P), M0)
+        Mt, _, U = O.scan(tail, *(cut(a, slice(t0, 40)) for a in P), Mp, log=True)
+        Mr = O.undo(tail, idx_w[:, :, t0:], U, Mt)
+        assert np.array_equal(Mr, Mp), t0

@@ -26,6 +26,9 @@
  *    range, a duplicate write slot, a wait that ran out) are recorded in a
  *    per-device status word that sdm_get_device_status() reads and clears.
  *  - Alignment: every tensor base must be 16-byte aligned.
+ *  - A call with no work (B, H or T zero) enqueues nothing and returns
+ *    SDM_OK after the shape check; its pointers are not looked at (empty
+ *    tensors may pass NULL).
  *  - The library allocates no device memory (the status word is a static
  *    device variable; scratch is the caller's `workspace`).  There is no
  *    CPU fallback.
@@ -155,6 +158,36 @@ sdm_status sdm_scan_noalloc(const sdm_shape* shape, const int32_t* idx_w,
                             const float* wt_w, const int32_t* idx_r,
                             const float* wt_r, const void* alpha, const void* beta,
                             const void* v, float* M, float* y, void* stream);
+
+/* sdm_scan that also keeps an undo log [SDM notes 2.9, appendix A.3: the
+ * forward pass writes the table in place and the backward pass brings back
+ * earlier states by undoing the sparse writes, for O(T*W*d_v) extra memory].
+ *   undo: [B,H,T,W,d_v] float32 out, caller-owned: undo[b,h,t,j,:] is the
+ *         value row idx_w[b,h,t,j] held just before step t's write (an
+ *         exact copy of the fp32 table row).
+ * All other arguments, the workspace and the results as in sdm_scan. */
+sdm_status sdm_scan_logged(const sdm_shape* shape, const int32_t* idx_w,
+                           const float* wt_w, const int32_t* idx_r,
+                           const float* wt_r, const void* alpha, const void* beta,
+                           const void* v, float* M, float* y, float* undo,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace sdm_scan_undo needs: B*H*N*4 (one mark per
+ * table row; 0 for an invalid shape). */
+size_t sdm_undo_workspace_size(const sdm_shape* shape);
+
+/* Undo a logged segment: M [B,H,N,d_v] float32, in place, goes back to the
+ * table it was before the sdm_scan_logged call that produced `undo` for the
+ * same idx_w [B,H,T,W] (shape->T = that segment's length).  Every row the
+ * segment wrote gets the copy logged at its earliest write; other rows are
+ * untouched.  The result is bit-exact.  Undoing segments in reverse order
+ * walks a long sequence back chunk by chunk.
+ *   workspace: at least sdm_undo_workspace_size(shape) bytes, caller-owned,
+ *   contents irrelevant on entry and on return.
+ * Slots outside [0, N) are skipped and recorded as SDM_ERR_DEVICE_BOUNDS. */
+sdm_status sdm_scan_undo(const sdm_shape* shape, const int32_t* idx_w,
+                         const float* undo, float* M, void* workspace,
+                         size_t ws_bytes, void* stream);
 
 /* One full forward step: sdm_address then sdm_scan on `stream`.
  * Inputs as above; M updated in place, y written, and the selected indices

@@ -25,7 +25,8 @@ STATUS = {0: "SDM_OK", 1: "SDM_ERR_INVALID_ARG", 2: "SDM_ERR_UNSUPPORTED", 3: "S
           4: "SDM_ERR_TIMEOUT", 5: "SDM_ERR_DEVICE_BOUNDS", 6: "SDM_ERR_DUPLICATE_SLOT"}
 
 EXPORTS = ["sdm_status_string", "sdm_subscores", "sdm_select", "sdm_address",
-           "sdm_workspace_size", "sdm_scan", "sdm_scan_noalloc", "sdm_forward",
+           "sdm_workspace_size", "sdm_scan", "sdm_scan_noalloc", "sdm_scan_logged",
+           "sdm_undo_workspace_size", "sdm_scan_undo", "sdm_forward",
            "sdm_get_device_status",
            "sdm_set_scan_tuning", "sdm_selftest_wait_timeout"]
 
@@ -85,6 +86,9 @@ def lib():
         "sdm_workspace_size": ([SP], ctypes.c_size_t),
         "sdm_scan": ([SP] + [P] * 10 + [ctypes.c_size_t, P], I),
         "sdm_scan_noalloc": ([SP] + [P] * 10, I),
+        "sdm_scan_logged": ([SP] + [P] * 11 + [ctypes.c_size_t, P], I),
+        "sdm_undo_workspace_size": ([SP], ctypes.c_size_t),
+        "sdm_scan_undo": ([SP, P, P, P, P, ctypes.c_size_t, P], I),
         "sdm_forward": ([SP] + [P] * 13 + [ctypes.c_size_t, P], I),
         "sdm_get_device_status": ([P], I),
         "sdm_set_scan_tuning": ([I, I], I),
@@ -218,6 +222,44 @@ def sdm_scan_noalloc(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y=N
                                _ptr(beta, "beta", dt), _ptr(v, "v", dt), _ptr(M, "M", f32),
                                _ptr(y, "y", f32), _stream(stream)), "sdm_scan_noalloc")
     return y
+
+
+def sdm_scan_logged(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y=None,
+                    undo=None, workspace=None, stream=None):
+    """sdm_scan that also logs each step's pre-write rows; M updated in place.
+    Returns (y, undo) with undo float32 [B,H,T,W,d_v]."""
+    if y is None:
+        y = _empty((sh.B, sh.H, sh.T, sh.d_v), torch.float32, M)
+    if undo is None:
+        undo = _empty((sh.B, sh.H, sh.T, sh.W, sh.d_v), torch.float32, M)
+    ws, nws = _workspace(sh, M, workspace)
+    dt, f32, i32 = _in_dt(sh), (torch.float32,), (torch.int32,)
+    _ok(lib().sdm_scan_logged(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32),
+                              _ptr(wt_w, "wt_w", f32), _ptr(idx_r, "idx_r", i32),
+                              _ptr(wt_r, "wt_r", f32), _ptr(alpha, "alpha", dt),
+                              _ptr(beta, "beta", dt), _ptr(v, "v", dt), _ptr(M, "M", f32),
+                              _ptr(y, "y", f32), _ptr(undo, "undo", f32), _ptr(ws, "workspace"),
+                              nws, _stream(stream)), "sdm_scan_logged")
+    return y, undo
+
+
+def sdm_undo_workspace_size(sh: Shape) -> int:
+    """Bytes of device workspace sdm_scan_undo needs for this shape."""
+    return int(lib().sdm_undo_workspace_size(ctypes.byref(sh)))
+
+
+def sdm_scan_undo(sh: Shape, idx_w, undo, M, workspace=None, stream=None):
+    """Put M back to the table before the logged segment (in place); returns M."""
+    if workspace is None:
+        workspace = torch.empty(max(sdm_undo_workspace_size(sh), 16), dtype=torch.uint8,
+                                device=M.device)
+    nws = workspace.numel() * workspace.element_size()
+    f32, i32 = (torch.float32,), (torch.int32,)
+    _ok(lib().sdm_scan_undo(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32),
+                            _ptr(undo, "undo", f32), _ptr(M, "M", f32),
+                            _ptr(workspace, "workspace"), nws, _stream(stream)),
+        "sdm_scan_undo")
+    return M
 
 
 def sdm_forward(sh: Shape, q_w, q_r, K, alpha, beta, v, M, y=None, idx_w=None, wt_w=None,

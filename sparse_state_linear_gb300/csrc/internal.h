@@ -36,10 +36,17 @@ cudaError_t launch_address(int mode, const Dims& d, const void* q0, const void* 
 // Scan (scan.cu): the plan kernel (writes per-row source codes into
 // `workspace`) then the scan kernel.
 size_t scan_workspace_bytes(const Dims& d);
+// `undo` (may be null): log of each step's pre-write rows [B,H,T,W,d_v].
 cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
                         const int32_t* idx_r, const float* wt_r, const void* alpha,
-                        const void* beta, const void* v, float* M, float* y, void* workspace,
-                        int depth, int col_slice, unsigned* status, cudaStream_t stream);
+                        const void* beta, const void* v, float* M, float* y, float* undo,
+                        void* workspace, int depth, int col_slice, unsigned* status,
+                        cudaStream_t stream);
+
+// Undo of a logged segment (scan.cu): `workspace` holds B*H*N marks.
+size_t undo_workspace_bytes(const Dims& d);
+cudaError_t launch_undo(const Dims& d, const int32_t* idx_w, const float* undo, float* M,
+                        void* workspace, unsigned* status, cudaStream_t stream);
 
 // Accessors of the API layer (sdm_api.cu) for other entry points.
 sdm_status api_check_shape(const sdm_shape* shape, Dims* d);

@@ -11,6 +11,11 @@
 // It needs the whole write set before any row is written: one more block
 // reduction per step.
 //
+// With an undo log ([SDM notes] 2.9, appendix A.3: the backward pass
+// restores earlier states by undoing the in-place sparse writes), the scan
+// also stores each write row's value from just before its step's write, and
+// undo_* below puts a segment's logged rows back.
+//
 // Parallel units: (chain = (b,h), column slice of CW floats).  The update
 // acts column by column with per-row scalars, so slices of one chain never
 // communicate, and a step's write slots are distinct, so no atomics.
@@ -85,6 +90,7 @@ struct ScanArgs {
   const int16_t* codes;
   float* M;
   float* y;
+  float* undo;      // optional log of the pre-write rows [B,H,T,W,d_v]
   int depth;
   unsigned* status;
 };
@@ -461,6 +467,8 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
           if (s & kSkip) continue;
           x = *reinterpret_cast<const float4*>(sm_c + (s & kOffMask));  // forwarded copy
         }
+        if (A.undo)
+          *reinterpret_cast<float4*>(A.undo + ((th0 + t) * W + j) * dv + c0 + 4 * myc) = x;
         const float cw = b * wj;
         float4 o;
         float mt_;
@@ -490,6 +498,8 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
           if (s & kSkip) continue;
           const float4 x = *reinterpret_cast<const float4*>(
               (s & kFwd) ? sm_c + (s & kOffMask) : wdst + j * rowb);
+          if (A.undo)
+            *reinterpret_cast<float4*>(A.undo + ((th0 + t) * W + j) * dv + c0 + 4 * myc) = x;
           const float wj = m->wt_w[j];
           md[pw] = make_float4(a * x.x, a * x.y, a * x.z, a * x.w);
           part.x = fmaf(wj, md[pw].x, part.x);
@@ -594,6 +604,64 @@ cudaError_t launch_t(const ScanArgs& A, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ undo
+// A logged segment is undone by putting back, for every row it wrote, the
+// copy logged at that row's earliest write in the segment.  Three passes
+// over the segment's write sets, as stream-ordered launches (no ordering
+// between steps is needed inside a pass):
+//   clear  mark[chain][row] = 0 for every row the segment wrote;
+//   mark   atomicMax(mark[chain][row], T - t), so the earliest step wins;
+//   copy   the (t, j) whose mark equals T - t copies its logged row back.
+struct UndoArgs {
+  const int32_t* idx_w;
+  const float* undo;
+  float* M;
+  uint32_t* mark;
+  long long n;          // B * H * T * W write entries
+  int T, W, dv;
+  uint32_t N;
+  unsigned* status;
+};
+
+constexpr int kUndoThreads = 256;
+
+__global__ void __launch_bounds__(kUndoThreads) undo_mark_kernel(const UndoArgs U, int pass) {
+  const long long stride = (long long)gridDim.x * kUndoThreads;
+  for (long long e = (long long)blockIdx.x * kUndoThreads + threadIdx.x; e < U.n; e += stride) {
+    const long long tw = (long long)U.T * U.W;
+    const long long chain = e / tw;
+    const int t = (int)((e - chain * tw) / U.W);
+    const int row = __ldg(U.idx_w + e);
+    if (row < 0 || (uint32_t)row >= U.N) {
+      if (pass == 1) record_status(U.status, SDM_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    uint32_t* mk = U.mark + chain * U.N + row;
+    if (pass == 0)
+      *mk = 0u;
+    else
+      atomicMax(mk, (uint32_t)(U.T - t));
+  }
+}
+
+// One warp per write entry: 16-byte copies of the logged row.
+__global__ void __launch_bounds__(kUndoThreads) undo_copy_kernel(const UndoArgs U) {
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (long long)gridDim.x * (kUndoThreads / 32);
+  const long long tw = (long long)U.T * U.W;
+  for (long long e = ((long long)blockIdx.x * kUndoThreads + threadIdx.x) >> 5; e < U.n;
+       e += nwarps) {
+    const long long chain = e / tw;
+    const int t = (int)((e - chain * tw) / U.W);
+    const int row = __ldg(U.idx_w + e);
+    if (row < 0 || (uint32_t)row >= U.N) continue;
+    if (U.mark[chain * U.N + row] != (uint32_t)(U.T - t)) continue;
+    const float4* src = reinterpret_cast<const float4*>(U.undo + e * U.dv);
+    float4* dst = reinterpret_cast<float4*>(U.M + (chain * U.N + row) * U.dv);
+    for (int c = lane; c < U.dv / 4; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
 constexpr size_t kSmemPerSM = 233472;   // 228 KiB
 constexpr size_t kSmemMaxCTA = 232448;  // 227 KiB
 constexpr int kSMs = 152;
@@ -606,8 +674,9 @@ size_t scan_workspace_bytes(const Dims& d) {
 
 cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
                         const int32_t* idx_r, const float* wt_r, const void* alpha,
-                        const void* beta, const void* v, float* M, float* y, void* workspace,
-                        int depth, int col_slice, unsigned* status, cudaStream_t stream) {
+                        const void* beta, const void* v, float* M, float* y, float* undo,
+                        void* workspace, int depth, int col_slice, unsigned* status,
+                        cudaStream_t stream) {
   const long long chains = (long long)d.B * d.H;
   if (chains == 0 || d.T == 0) return cudaSuccess;
   int cw = col_slice;
@@ -640,11 +709,31 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  ScanArgs A{d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, codes, M, y, D, status};
+  ScanArgs A{d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, codes, M, y, undo, D, status};
   const bool bf = d.in_dtype == SDM_BF16;
   if (cw == 64) return bf ? launch_t<64, true>(A, stream) : launch_t<64, false>(A, stream);
   if (cw == 32) return bf ? launch_t<32, true>(A, stream) : launch_t<32, false>(A, stream);
   return bf ? launch_t<16, true>(A, stream) : launch_t<16, false>(A, stream);
+}
+
+size_t undo_workspace_bytes(const Dims& d) {
+  return (size_t)d.B * d.H * (size_t)d.N() * sizeof(uint32_t);
+}
+
+cudaError_t launch_undo(const Dims& d, const int32_t* idx_w, const float* undo, float* M,
+                        void* workspace, unsigned* status, cudaStream_t stream) {
+  const long long n = (long long)d.B * d.H * d.T * d.W;
+  if (n == 0) return cudaSuccess;
+  UndoArgs U{idx_w, undo, M, static_cast<uint32_t*>(workspace), n, d.T, d.W, d.dv,
+             (uint32_t)d.N(), status};
+  const long long want = (n + kUndoThreads - 1) / kUndoThreads;
+  const unsigned blocks = (unsigned)(want < 8 * kSMs ? want : 8 * kSMs);
+  undo_mark_kernel<<<blocks, kUndoThreads, 0, stream>>>(U, 0);
+  undo_mark_kernel<<<blocks, kUndoThreads, 0, stream>>>(U, 1);
+  const long long wantc = (n + kUndoThreads / 32 - 1) / (kUndoThreads / 32);
+  const unsigned cblocks = (unsigned)(wantc < 16 * kSMs ? wantc : 16 * kSMs);
+  undo_copy_kernel<<<cblocks, kUndoThreads, 0, stream>>>(U);
+  return cudaGetLastError();
 }
 
 }  // namespace sdm

@@ -131,10 +131,10 @@ sdm_status sdm_subscores(const sdm_shape* shape, const void* q, const void* K, f
   Dims d;
   sdm_status st = check_shape(shape, &d);
   if (st != SDM_OK) return st;
+  if (empty_work(d)) return SDM_OK;   // no work: pointers are not looked at
   SDM_CHECK_PTR(q);
   SDM_CHECK_PTR(K);
   SDM_CHECK_PTR(S);
-  if (empty_work(d)) return SDM_OK;
   unsigned* sp = nullptr;
   if ((st = status_ptr(&sp)) != SDM_OK) return st;
   return from_cuda(launch_address(kAddrScoresOnly, d, q, nullptr, K, nullptr, nullptr,
@@ -148,13 +148,13 @@ sdm_status sdm_select(const sdm_shape* shape, const float* sub_w, const float* s
   Dims d;
   sdm_status st = check_shape(shape, &d);
   if (st != SDM_OK) return st;
+  if (empty_work(d)) return SDM_OK;   // no work: pointers are not looked at
   SDM_CHECK_PTR(sub_w);
   SDM_CHECK_PTR(sub_r);
   SDM_CHECK_PTR(idx_w);
   SDM_CHECK_PTR(wt_w);
   SDM_CHECK_PTR(idx_r);
   SDM_CHECK_PTR(wt_r);
-  if (empty_work(d)) return SDM_OK;
   unsigned* sp = nullptr;
   if ((st = status_ptr(&sp)) != SDM_OK) return st;
   return from_cuda(launch_address(kAddrSelectOnly, d, nullptr, nullptr, nullptr, sub_w,
@@ -168,6 +168,7 @@ sdm_status sdm_address(const sdm_shape* shape, const void* q_w, const void* q_r,
   Dims d;
   sdm_status st = check_shape(shape, &d);
   if (st != SDM_OK) return st;
+  if (empty_work(d)) return SDM_OK;   // no work: pointers are not looked at
   SDM_CHECK_PTR(q_w);
   SDM_CHECK_PTR(q_r);
   SDM_CHECK_PTR(K);
@@ -175,7 +176,6 @@ sdm_status sdm_address(const sdm_shape* shape, const void* q_w, const void* q_r,
   SDM_CHECK_PTR(wt_w);
   SDM_CHECK_PTR(idx_r);
   SDM_CHECK_PTR(wt_r);
-  if (empty_work(d)) return SDM_OK;
   unsigned* sp = nullptr;
   if ((st = status_ptr(&sp)) != SDM_OK) return st;
   return from_cuda(launch_address(kAddrFused, d, q_w, q_r, K, nullptr, nullptr, idx_w, wt_w,
@@ -188,13 +188,15 @@ size_t sdm_workspace_size(const sdm_shape* shape) {
   return scan_workspace_bytes(d);
 }
 
-sdm_status sdm_scan(const sdm_shape* shape, const int32_t* idx_w, const float* wt_w,
-                    const int32_t* idx_r, const float* wt_r, const void* alpha,
-                    const void* beta, const void* v, float* M, float* y, void* workspace,
-                    size_t ws_bytes, void* stream) {
+// sdm_scan and sdm_scan_logged: `undo` is null for the plain scan.
+static sdm_status scan_entry(const sdm_shape* shape, const int32_t* idx_w, const float* wt_w,
+                             const int32_t* idx_r, const float* wt_r, const void* alpha,
+                             const void* beta, const void* v, float* M, float* y, float* undo,
+                             bool logged, void* workspace, size_t ws_bytes, void* stream) {
   Dims d;
   sdm_status st = check_shape(shape, &d);
   if (st != SDM_OK) return st;
+  if (empty_work(d)) return SDM_OK;   // no work: pointers are not looked at
   SDM_CHECK_PTR(idx_w);
   SDM_CHECK_PTR(wt_w);
   SDM_CHECK_PTR(idx_r);
@@ -204,7 +206,7 @@ sdm_status sdm_scan(const sdm_shape* shape, const int32_t* idx_w, const float* w
   SDM_CHECK_PTR(v);
   SDM_CHECK_PTR(M);
   SDM_CHECK_PTR(y);
-  if (empty_work(d)) return SDM_OK;
+  if (logged) SDM_CHECK_PTR(undo);
   SDM_CHECK_PTR(workspace);
   if (ws_bytes < scan_workspace_bytes(d)) return SDM_ERR_INVALID_ARG;
   unsigned* sp = nullptr;
@@ -216,8 +218,47 @@ sdm_status sdm_scan(const sdm_shape* shape, const int32_t* idx_w, const float* w
     cs = g_colslice;
   }
   if (cs && d.dv % cs != 0) return SDM_ERR_INVALID_ARG;
-  return from_cuda(launch_scan(d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, workspace,
-                               depth, cs, sp, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_scan(d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, undo,
+                               workspace, depth, cs, sp, static_cast<cudaStream_t>(stream)));
+}
+
+sdm_status sdm_scan(const sdm_shape* shape, const int32_t* idx_w, const float* wt_w,
+                    const int32_t* idx_r, const float* wt_r, const void* alpha,
+                    const void* beta, const void* v, float* M, float* y, void* workspace,
+                    size_t ws_bytes, void* stream) {
+  return scan_entry(shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, nullptr, false,
+                    workspace, ws_bytes, stream);
+}
+
+sdm_status sdm_scan_logged(const sdm_shape* shape, const int32_t* idx_w, const float* wt_w,
+                           const int32_t* idx_r, const float* wt_r, const void* alpha,
+                           const void* beta, const void* v, float* M, float* y, float* undo,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  return scan_entry(shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, undo, true,
+                    workspace, ws_bytes, stream);
+}
+
+size_t sdm_undo_workspace_size(const sdm_shape* shape) {
+  Dims d;
+  if (check_shape(shape, &d) != SDM_OK) return 0;
+  return undo_workspace_bytes(d);
+}
+
+sdm_status sdm_scan_undo(const sdm_shape* shape, const int32_t* idx_w, const float* undo,
+                         float* M, void* workspace, size_t ws_bytes, void* stream) {
+  Dims d;
+  sdm_status st = check_shape(shape, &d);
+  if (st != SDM_OK) return st;
+  if (empty_work(d)) return SDM_OK;   // no work: pointers are not looked at
+  SDM_CHECK_PTR(idx_w);
+  SDM_CHECK_PTR(undo);
+  SDM_CHECK_PTR(M);
+  SDM_CHECK_PTR(workspace);
+  if (ws_bytes < undo_workspace_bytes(d)) return SDM_ERR_INVALID_ARG;
+  unsigned* sp = nullptr;
+  if ((st = status_ptr(&sp)) != SDM_OK) return st;
+  return from_cuda(launch_undo(d, idx_w, undo, M, workspace, sp,
+                               static_cast<cudaStream_t>(stream)));
 }
 
 sdm_status sdm_forward(const sdm_shape* shape, const void* q_w, const void* q_r,
@@ -228,15 +269,14 @@ sdm_status sdm_forward(const sdm_shape* shape, const void* q_w, const void* q_r,
   Dims d;
   sdm_status st = check_shape(shape, &d);
   if (st != SDM_OK) return st;
+  if (empty_work(d)) return SDM_OK;   // no work: pointers are not looked at
   SDM_CHECK_PTR(alpha);
   SDM_CHECK_PTR(beta);
   SDM_CHECK_PTR(v);
   SDM_CHECK_PTR(M);
   SDM_CHECK_PTR(y);
-  if (!empty_work(d)) {
-    SDM_CHECK_PTR(workspace);
-    if (ws_bytes < scan_workspace_bytes(d)) return SDM_ERR_INVALID_ARG;
-  }
+  SDM_CHECK_PTR(workspace);
+  if (ws_bytes < scan_workspace_bytes(d)) return SDM_ERR_INVALID_ARG;
   st = sdm_address(shape, q_w, q_r, K, idx_w, wt_w, idx_r, wt_r, stream);
   if (st != SDM_OK) return st;
   return sdm_scan(shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, workspace, ws_bytes,

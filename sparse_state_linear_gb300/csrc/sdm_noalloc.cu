@@ -55,10 +55,10 @@ extern "C" sdm_status sdm_scan_noalloc(const sdm_shape* shape, const int32_t* id
   Dims d;
   sdm_status st = api_check_shape(shape, &d);
   if (st != SDM_OK) return st;
+  if ((long long)d.B * d.H * d.T == 0) return SDM_OK;   // no work: pointers are not looked at
   const void* ptrs[] = {idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return SDM_ERR_INVALID_ARG;
-  if ((long long)d.B * d.H * d.T == 0) return SDM_OK;
   // Problems whose plan codes do not fit the fixed scratch are refused.
   if (scan_workspace_bytes(d) > kNoAllocScratchBytes) return SDM_ERR_UNSUPPORTED;
   void* scratch = nullptr;
@@ -70,7 +70,8 @@ extern "C" sdm_status sdm_scan_noalloc(const sdm_shape* shape, const int32_t* id
   if (col_slice && d.dv % col_slice != 0) return SDM_ERR_INVALID_ARG;
   // Every code the scan reads is written by the plan kernel of this same
   // call, so nothing in the scratch has to start at zero.
-  const cudaError_t e = launch_scan(d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, scratch,
-                                    depth, col_slice, status, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_scan(d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, nullptr,
+                                    scratch, depth, col_slice, status,
+                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;
 }

@@ -87,12 +87,49 @@ def test_null_and_misaligned_pointers(L):
     assert L.sdm_workspace_size(ctypes.byref(good_shape(W=0))) == 0
 
 
+def test_logged_scan_and_undo_arguments(L):
+    sh = good_shape()
+    need = L.sdm_workspace_size(ctypes.byref(sh))
+    # sdm_scan_logged: the ten tensors (undo last) must be present and aligned.
+    for i in range(10):
+        p = [FAKE] * 10
+        p[i] = None
+        assert L.sdm_scan_logged(ctypes.byref(sh), *p, FAKE, need, None) == 1
+        p[i] = MISALIGNED
+        assert L.sdm_scan_logged(ctypes.byref(sh), *p, FAKE, need, None) == 1
+    assert L.sdm_scan_logged(ctypes.byref(sh), *([FAKE] * 10), FAKE, need - 1, None) == 1
+    # sdm_scan_undo: one mark per table row of every chain.
+    uneed = L.sdm_undo_workspace_size(ctypes.byref(sh))
+    assert uneed == sh.B * sh.H * sh.N * 4
+    assert L.sdm_undo_workspace_size(ctypes.byref(good_shape(W=0))) == 0
+    for i in range(3):
+        p = [FAKE] * 3
+        p[i] = None
+        assert L.sdm_scan_undo(ctypes.byref(sh), *p, FAKE, uneed, None) == 1
+        p[i] = MISALIGNED
+        assert L.sdm_scan_undo(ctypes.byref(sh), *p, FAKE, uneed, None) == 1
+    assert L.sdm_scan_undo(ctypes.byref(sh), FAKE, FAKE, FAKE, None, uneed, None) == 1
+    assert L.sdm_scan_undo(ctypes.byref(sh), FAKE, FAKE, FAKE, FAKE, uneed - 1, None) == 1
+    assert L.sdm_scan_undo(ctypes.byref(good_shape(n_sub=600)), FAKE, FAKE, FAKE, FAKE,
+                           uneed, None) == 2
+    # Empty segments return before any CUDA call.
+    for kw in (dict(T=0), dict(B=0)):
+        e = good_shape(**kw)
+        assert L.sdm_scan_undo(ctypes.byref(e), FAKE, FAKE, FAKE, None, 0, None) == 0
+        assert L.sdm_scan_logged(ctypes.byref(e), *([FAKE] * 10), None, 0, None) == 0
+
+
 def test_empty_work_is_a_no_op(L):
     # Nothing to do: returns before any CUDA call, so it works without a GPU.
     for kw in (dict(T=0), dict(B=0), dict(H=0)):
         sh = good_shape(**kw)
         assert scan_rc(L, sh) == 0
         assert L.sdm_forward(ctypes.byref(sh), *([FAKE] * 12), FAKE, 0, None) == 0
+        # Empty tensors may come as NULL pointers.
+        assert scan_rc(L, sh, [None] * 9) == 0
+        assert L.sdm_forward(ctypes.byref(sh), *([None] * 13), 0, None) == 0
+        assert L.sdm_address(ctypes.byref(sh), *([None] * 7), None) == 0
+        assert L.sdm_scan_noalloc(ctypes.byref(sh), *([None] * 9), None) == 0
 
 
 def test_tuning_arguments(L):

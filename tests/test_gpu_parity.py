@@ -428,3 +428,73 @@ def test_bounded_wait_reports_timeout():
     sdm.sdm_selftest_wait_timeout(50_000_000)
     assert sdm.sdm_get_device_status() == 4
     status_ok()
+
+
+# ------------------------------------------------------------------ undo log
+
+UNDO_CASES = [  # B, H, T, s, dv, W, R, bf16
+    (1, 2, 120, 4, 32, 8, 8, False),       # N = 16: rows rewritten again and again
+    (2, 1, 90, 16, 64, 32, 16, True),
+    (1, 1, 60, 32, 128, 64, 64, True),
+]
+
+
+@pytest.mark.parametrize("form", [0, 1])
+@pytest.mark.parametrize("B,H,T,s,dv,W,R,bf16", UNDO_CASES)
+def test_scan_logged_matches_oracle(B, H, T, s, dv, W, R, bf16, form):
+    rng = np.random.default_rng(300 + T + W + form)
+    case = random_scan_case(rng, B, H, T, s, dv, W, R, bf16)
+    idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0 = case
+    sh_g = sdm.make_shape(B, H, T, s, 16, dv, W, R,
+                          in_dtype=sdm.SDM_BF16 if bf16 else sdm.SDM_F32, update=form)
+    dev = lambda a: torch.from_numpy(a).to(DEV)
+    M = dev(M0)
+    y, U = sdm.sdm_scan_logged(sh_g, dev(idx_w), dev(wt_w), dev(idx_r), dev(wt_r),
+                               alpha.to(DEV), beta.to(DEV), v.to(DEV), M)
+    status_ok()
+    # Logging does not change the arithmetic.
+    Mp, yp = run_scan(sh_g, case)
+    assert np.array_equal(M.cpu().numpy(), Mp) and np.array_equal(y.cpu().numpy(), yp)
+    sh_o = O.Shape(B=B, H=H, T=T, n_sub=s, d_h=16, d_v=dv, W=W, R=R, update_form=form)
+    Mo, yo, Uo = O.scan(sh_o, idx_w, wt_w.astype(np.float64), idx_r, wt_r.astype(np.float64),
+                        np32(alpha), np32(beta), np32(v), M0, log=True)
+    assert max_rel(np32(U), Uo) <= FTOL
+    assert max_rel(np32(y), yo) <= FTOL
+
+
+@pytest.mark.parametrize("form", [0, 1])
+@pytest.mark.parametrize("B,H,T,s,dv,W,R,bf16", UNDO_CASES)
+def test_undo_restores_bit_exactly(B, H, T, s, dv, W, R, bf16, form):
+    rng = np.random.default_rng(400 + T + W + form)
+    case = random_scan_case(rng, B, H, T, s, dv, W, R, bf16)
+    idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0 = case
+    dt = sdm.SDM_BF16 if bf16 else sdm.SDM_F32
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    gates = [alpha.to(DEV), beta.to(DEV), v.to(DEV)]
+    for t0 in (0, T // 3, T - 1):
+        pre = sdm.make_shape(B, H, t0, s, 16, dv, W, R, in_dtype=dt, update=form)
+        tail = sdm.make_shape(B, H, T - t0, s, 16, dv, W, R, in_dtype=dt, update=form)
+        M = dev(M0)
+        cut = lambda a, sl: a[:, :, sl].clone() if torch.is_tensor(a) else dev(a[:, :, sl])
+        P = (idx_w, wt_w, idx_r, wt_r)
+        sdm.sdm_scan(pre, *(cut(a, slice(0, t0)) for a in P), *(cut(g, slice(0, t0)) for g in gates), M)
+        Mp = M.clone()
+        _, U = sdm.sdm_scan_logged(tail, *(cut(a, slice(t0, T)) for a in P),
+                                   *(cut(g, slice(t0, T)) for g in gates), M)
+        assert not torch.equal(M, Mp)
+        sdm.sdm_scan_undo(tail, cut(idx_w, slice(t0, T)), U, M)
+        status_ok()
+        assert torch.equal(M, Mp), t0
+
+
+def test_undo_reports_bad_slots():
+    B, H, T, s, dv, W = 1, 1, 4, 4, 16, 2
+    sh_g = sdm.make_shape(B, H, T, s, 16, dv, W, 1, in_dtype=sdm.SDM_F32)
+    idx = torch.tensor([[[[0, 1], [2, 16], [3, 0], [1, 2]]]], dtype=torch.int32, device=DEV)
+    U = torch.zeros(B, H, T, W, dv, device=DEV)
+    M = torch.ones(B, H, s * s, dv, device=DEV)
+    sdm.sdm_scan_undo(sh_g, idx, U, M)
+    assert sdm.sdm_get_device_status() == 5
+    # The valid rows were still restored (rows 0-3 each from their earliest write).
+    assert torch.equal(M[0, 0, :4], torch.zeros(4, dv, device=DEV))
+    assert torch.equal(M[0, 0, 4:], torch.ones(s * s - 4, dv, device=DEV))

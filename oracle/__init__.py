@@ -86,8 +86,10 @@ def _L():
         _lib.sdm_ref_forward.argtypes = [sp] + [P] * 12
         _lib.sdm_ref_scan_logged.argtypes = [sp] + [P] * 10
         _lib.sdm_ref_undo.argtypes = [sp] + [P] * 3
+        _lib.sdm_ref_rmsnorm_gate.argtypes = [sp, P, P, P, ctypes.c_double, P]
         for f in (_lib.sdm_ref_subscores, _lib.sdm_ref_select, _lib.sdm_ref_scan,
-                  _lib.sdm_ref_forward, _lib.sdm_ref_scan_logged, _lib.sdm_ref_undo):
+                  _lib.sdm_ref_forward, _lib.sdm_ref_scan_logged, _lib.sdm_ref_undo,
+                  _lib.sdm_ref_rmsnorm_gate):
             f.restype = ctypes.c_int
     return _lib
 
@@ -174,6 +176,24 @@ def undo(sh: Shape, idx_w, U, M1):
     cs = sh.c()
     _check(_L().sdm_ref_undo(ctypes.byref(cs), _p(idx_w), _p(U), _p(M)), "undo")
     return M
+
+
+def rmsnorm_gate(sh: Shape, y, g, gamma=None, eps: float = 1e-6):
+    """Per-head RMS-Norm and output gate: y [B,H,T,d_v], g [B,H,T,d_v],
+    gamma [H,d_v] or None -> float64 [B,H,T,d_v]."""
+    y = _arr(y, np.float64)
+    g = _arr(g, np.float32)
+    assert y.shape == (sh.B, sh.H, sh.T, sh.d_v) and g.shape == y.shape
+    gp = None
+    if gamma is not None:
+        gamma = _arr(gamma, np.float32)
+        assert gamma.shape == (sh.H, sh.d_v)
+        gp = _p(gamma)
+    out = np.empty(y.shape, np.float64)
+    cs = sh.c()
+    _check(_L().sdm_ref_rmsnorm_gate(ctypes.byref(cs), _p(y), _p(g), gp, float(eps), _p(out)),
+           "rmsnorm_gate")
+    return out
 
 
 def forward(sh: Shape, q_w, q_r, K, alpha, beta, v, M0):

@@ -259,6 +259,30 @@ extern "C" int sdm_ref_undo(const sdm_ref_shape* sh, const int32_t* idx_w,
   return 0;
 }
 
+// [SDM notes] 2.4, after Eq. (5): each head's read result goes through an
+// RMS-Norm and an element-wise output gate (the head-mixing projection W_o
+// that follows is not part of this step).  RMSNorm(y) = y / sqrt(mean(y^2)
+// + eps) times a per-head learned scale gamma[h,:]; the gate g is applied as
+// given.
+extern "C" int sdm_ref_rmsnorm_gate(const sdm_ref_shape* sh, const double* y,
+                                    const float* g, const float* gamma, double eps,
+                                    double* out) {
+  if (!shape_ok(sh) || !y || !g || !out || !(eps > 0.0)) return -1;
+  const int H = sh->H, T = sh->T, dv = sh->d_v;
+  for (size_t row = 0; row < (size_t)sh->B * H * T; ++row) {
+    const int h = (int)((row / T) % H);
+    const double* yr = y + row * dv;
+    double ss = 0.0;
+    for (int c = 0; c < dv; ++c) ss += yr[c] * yr[c];
+    const double inv = 1.0 / std::sqrt(ss / dv + eps);
+    for (int c = 0; c < dv; ++c) {
+      const double sc = gamma ? (double)gamma[(size_t)h * dv + c] : 1.0;
+      out[row * dv + c] = yr[c] * inv * sc * (double)g[row * dv + c];
+    }
+  }
+  return 0;
+}
+
 extern "C" int sdm_ref_forward(const sdm_ref_shape* sh, const float* q_w,
                                const float* q_r, const float* K,
                                const float* alpha, const float* beta,

@@ -81,6 +81,12 @@ int sdm_ref_scan_logged(const sdm_ref_shape* sh,
 int sdm_ref_undo(const sdm_ref_shape* sh, const int32_t* idx_w,
                  const double* undo, double* M);
 
+/* Per-head RMS-Norm and element-wise output gate on the read result:
+ * out = y / sqrt(mean_c y^2 + eps) * gamma[h,:] * g.  y, out: [B,H,T,d_v]
+ * (double); g: [B,H,T,d_v] float; gamma: [H,d_v] float or NULL (ones). */
+int sdm_ref_rmsnorm_gate(const sdm_ref_shape* sh, const double* y, const float* g,
+                         const float* gamma, double eps, double* out);
+
 /* Sub-scores, both selections and the scan, in that order.  The selected
  * indices and weights are returned too (none of the idx and wt outputs may be NULL). */
 int sdm_ref_forward(const sdm_ref_shape* sh,

@@ -422,3 +422,33 @@ def test_undo_restores_the_segment_start(oracle_mod, form):
         Mt, _, U = O.scan(tail, *(cut(a, slice(t0, 40)) for a in P), Mp, log=True)
         Mr = O.undo(tail, idx_w[:, :, t0:], U, Mt)
         assert np.array_equal(Mr, Mp), t0
+
+
+# ------------------------------------------------------------------ epilogue
+# [SDM notes] 2.4, after Eq. (5): per-head RMS-Norm, then the element-wise
+# output gate.
+
+def test_rmsnorm_gate_unit_rms_and_closed_forms(oracle_mod):
+    rng = np.random.default_rng(31)
+    shape = sh(B=2, H=3, T=5, d_v=12)
+    y = rng.standard_normal((2, 3, 5, 12))
+    ones = np.ones((2, 3, 5, 12), np.float32)
+    out = O.rmsnorm_gate(shape, y, ones, eps=1e-300)
+    # Unit RMS per (b, h, t) row, direction kept.
+    assert np.allclose(np.sqrt(np.mean(out ** 2, axis=-1)), 1.0, rtol=1e-12)
+    assert np.allclose(out * np.linalg.norm(y, axis=-1, keepdims=True),
+                       y * np.sqrt(12), rtol=1e-12)
+    # Scale invariance of the norm and linearity in the gate and in gamma.
+    assert np.allclose(O.rmsnorm_gate(shape, 7.5 * y, ones, eps=1e-300), out, rtol=1e-12)
+    g = rng.uniform(-2, 2, (2, 3, 5, 12)).astype(np.float32)
+    gamma = rng.uniform(0.5, 1.5, (3, 12)).astype(np.float32)
+    full = O.rmsnorm_gate(shape, y, g, gamma, eps=1e-300)
+    assert np.allclose(full, out * g * gamma[None, :, None, :], rtol=1e-12)
+    # A constant row c gives c / sqrt(c^2 + eps) in every column.
+    c = np.full((2, 3, 5, 12), 0.25)
+    got = O.rmsnorm_gate(shape, c, ones, eps=0.0625)
+    assert np.allclose(got, 0.25 / np.sqrt(0.0625 + 0.0625), rtol=1e-14)
+    # Each head uses its own gamma row.
+    gh = np.zeros((3, 12), np.float32); gh[1] = 1.0
+    only1 = O.rmsnorm_gate(shape, y, ones, gh, eps=1e-300)
+    assert np.all(only1[:, [0, 2]] == 0) and np.allclose(only1[:, 1], out[:, 1], rtol=1e-12)

@@ -189,6 +189,21 @@ sdm_status sdm_scan_undo(const sdm_shape* shape, const int32_t* idx_w,
                          const float* undo, float* M, void* workspace,
                          size_t ws_bytes, void* stream);
 
+/* Per-head RMS-Norm and element-wise output gate on the read result
+ * [SDM notes 2.4, after Eq. (5); the head-mixing projection that follows is
+ * not part of this library]:
+ *   out[b,h,t,:] = y[b,h,t,:] / sqrt(mean_c y[b,h,t,c]^2 + eps)
+ *                  * gamma[h,:] * g[b,h,t,:]
+ *   y:     [B,H,T,d_v] float32 (the scan's output);
+ *   g:     [B,H,T,d_v] output gate, in shape->in_dtype, applied as given;
+ *   gamma: [H,d_v] float32 per-head scale, or NULL for ones;
+ *   eps:   > 0;  out: [B,H,T,d_v] in out_dtype (SDM_BF16 or SDM_F32).
+ * One pass over y, bandwidth-bound.  Shape fields other than B, H, T, d_v
+ * and in_dtype only need to be valid. */
+sdm_status sdm_rmsnorm_gate(const sdm_shape* shape, const float* y, const void* g,
+                            const float* gamma, float eps, void* out,
+                            sdm_dtype out_dtype, void* stream);
+
 /* One full forward step: sdm_address then sdm_scan on `stream`.
  * Inputs as above; M updated in place, y written, and the selected indices
  * and weights returned in the caller's idx_w/wt_w/idx_r/wt_r buffers. */

@@ -26,7 +26,7 @@ STATUS = {0: "SDM_OK", 1: "SDM_ERR_INVALID_ARG", 2: "SDM_ERR_UNSUPPORTED", 3: "S
 
 EXPORTS = ["sdm_status_string", "sdm_subscores", "sdm_select", "sdm_address",
            "sdm_workspace_size", "sdm_scan", "sdm_scan_noalloc", "sdm_scan_logged",
-           "sdm_undo_workspace_size", "sdm_scan_undo", "sdm_forward",
+           "sdm_undo_workspace_size", "sdm_scan_undo", "sdm_rmsnorm_gate", "sdm_forward",
            "sdm_get_device_status",
            "sdm_set_scan_tuning", "sdm_selftest_wait_timeout"]
 
@@ -89,6 +89,7 @@ def lib():
         "sdm_scan_logged": ([SP] + [P] * 11 + [ctypes.c_size_t, P], I),
         "sdm_undo_workspace_size": ([SP], ctypes.c_size_t),
         "sdm_scan_undo": ([SP, P, P, P, P, ctypes.c_size_t, P], I),
+        "sdm_rmsnorm_gate": ([SP, P, P, P, ctypes.c_float, P, I, P], I),
         "sdm_forward": ([SP] + [P] * 13 + [ctypes.c_size_t, P], I),
         "sdm_get_device_status": ([P], I),
         "sdm_set_scan_tuning": ([I, I], I),
@@ -260,6 +261,21 @@ def sdm_scan_undo(sh: Shape, idx_w, undo, M, workspace=None, stream=None):
                             _ptr(workspace, "workspace"), nws, _stream(stream)),
         "sdm_scan_undo")
     return M
+
+
+def sdm_rmsnorm_gate(sh: Shape, y, g, gamma=None, eps: float = 1e-6, out=None,
+                     out_dtype=SDM_BF16, stream=None):
+    """Per-head RMS-Norm and output gate on y [B,H,T,d_v] float32; g in the
+    shape's input dtype; gamma [H,d_v] float32 or None.  Returns out."""
+    tdt = torch.bfloat16 if out_dtype == SDM_BF16 else torch.float32
+    if out is None:
+        out = _empty((sh.B, sh.H, sh.T, sh.d_v), tdt, y)
+    f32 = (torch.float32,)
+    gp = None if gamma is None else _ptr(gamma, "gamma", f32)
+    _ok(lib().sdm_rmsnorm_gate(ctypes.byref(sh), _ptr(y, "y", f32), _ptr(g, "g", _in_dt(sh)), gp,
+                               float(eps), _ptr(out, "out", (tdt,)), int(out_dtype),
+                               _stream(stream)), "sdm_rmsnorm_gate")
+    return out
 
 
 def sdm_forward(sh: Shape, q_w, q_r, K, alpha, beta, v, M, y=None, idx_w=None, wt_w=None,

@@ -48,6 +48,11 @@ size_t undo_workspace_bytes(const Dims& d);
 cudaError_t launch_undo(const Dims& d, const int32_t* idx_w, const float* undo, float* M,
                         void* workspace, unsigned* status, cudaStream_t stream);
 
+// Per-head RMS-Norm and output gate on y (epilogue.cu).  g has d.in_dtype;
+// out_dtype is SDM_F32 or SDM_BF16; gamma may be null.
+cudaError_t launch_rmsnorm_gate(const Dims& d, const float* y, const void* g, const float* gamma,
+                                float eps, void* out, int out_dtype, cudaStream_t stream);
+
 // Accessors of the API layer (sdm_api.cu) for other entry points.
 sdm_status api_check_shape(const sdm_shape* shape, Dims* d);
 sdm_status api_status_ptr(unsigned** out);

@@ -283,6 +283,23 @@ sdm_status sdm_forward(const sdm_shape* shape, const void* q_w, const void* q_r,
                   stream);
 }
 
+sdm_status sdm_rmsnorm_gate(const sdm_shape* shape, const float* y, const void* g,
+                            const float* gamma, float eps, void* out, sdm_dtype out_dtype,
+                            void* stream) {
+  Dims d;
+  sdm_status st = check_shape(shape, &d);
+  if (st != SDM_OK) return st;
+  if (!(eps > 0.f) || !(eps < INFINITY)) return SDM_ERR_INVALID_ARG;
+  if (out_dtype != SDM_F32 && out_dtype != SDM_BF16) return SDM_ERR_INVALID_ARG;
+  if (empty_work(d)) return SDM_OK;   // no work: pointers are not looked at
+  SDM_CHECK_PTR(y);
+  SDM_CHECK_PTR(g);
+  SDM_CHECK_PTR(out);
+  if (gamma && !aligned16(gamma)) return SDM_ERR_INVALID_ARG;
+  return from_cuda(launch_rmsnorm_gate(d, y, g, gamma, eps, out, out_dtype,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 sdm_status sdm_get_device_status(void* stream) {
   unsigned* sp = nullptr;
   sdm_status st = status_ptr(&sp);

@@ -119,6 +119,21 @@ def test_logged_scan_and_undo_arguments(L):
         assert L.sdm_scan_logged(ctypes.byref(e), *([FAKE] * 10), None, 0, None) == 0
 
 
+def test_rmsnorm_gate_arguments(L):
+    sh = good_shape()
+    rc = lambda *a: L.sdm_rmsnorm_gate(ctypes.byref(sh), *a)
+    assert rc(FAKE, FAKE, None, ctypes.c_float(0.0), FAKE, 1, None) == 1          # eps
+    assert rc(FAKE, FAKE, None, ctypes.c_float(float("inf")), FAKE, 1, None) == 1
+    assert rc(FAKE, FAKE, None, ctypes.c_float(1e-6), FAKE, 7, None) == 1         # out dtype
+    assert rc(None, FAKE, None, ctypes.c_float(1e-6), FAKE, 1, None) == 1
+    assert rc(FAKE, MISALIGNED, None, ctypes.c_float(1e-6), FAKE, 1, None) == 1
+    assert rc(FAKE, FAKE, MISALIGNED, ctypes.c_float(1e-6), FAKE, 1, None) == 1
+    assert rc(FAKE, FAKE, None, ctypes.c_float(1e-6), None, 0, None) == 1
+    e = good_shape(T=0)
+    assert L.sdm_rmsnorm_gate(ctypes.byref(e), None, None, None, ctypes.c_float(1e-6), None, 1,
+                              None) == 0
+
+
 def test_empty_work_is_a_no_op(L):
     # Nothing to do: returns before any CUDA call, so it works without a GPU.
     for kw in (dict(T=0), dict(B=0), dict(H=0)):

@@ -498,3 +498,51 @@ def test_undo_reports_bad_slots():
     # The valid rows were still restored (rows 0-3 each from their earliest write).
     assert torch.equal(M[0, 0, :4], torch.zeros(4, dv, device=DEV))
     assert torch.equal(M[0, 0, 4:], torch.ones(s * s - 4, dv, device=DEV))
+
+
+# ------------------------------------------------------------------ epilogue
+
+@pytest.mark.parametrize("B,H,T,dv,bf16", [(2, 3, 37, 128, True), (1, 2, 5, 16, False),
+                                           (1, 2, 9, 1920, True), (3, 1, 64, 960, False)])
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_rmsnorm_gate_matches_oracle(B, H, T, dv, bf16, out_dtype):
+    rng = np.random.default_rng(B * 100 + dv + out_dtype)
+    y = (rng.standard_normal((B, H, T, dv)) * rng.uniform(0.01, 3, (B, H, T, 1))).astype(np.float32)
+    g32 = rng.uniform(-1.5, 1.5, (B, H, T, dv)).astype(np.float32)
+    gamma = rng.uniform(0.5, 1.5, (H, dv)).astype(np.float32)
+    dt = torch.bfloat16 if bf16 else torch.float32
+    g = torch.from_numpy(g32).to(dt)
+    sh_g = sdm.make_shape(B, H, T, 16, 16, dv, 1, 1, in_dtype=sdm.SDM_BF16 if bf16 else sdm.SDM_F32)
+    out = sdm.sdm_rmsnorm_gate(sh_g, torch.from_numpy(y).to(DEV), g.to(DEV),
+                               torch.from_numpy(gamma).to(DEV), eps=1e-6, out_dtype=out_dtype)
+    status_ok()
+    sh_o = O.Shape(B=B, H=H, T=T, n_sub=16, d_h=16, d_v=dv, W=1, R=1)
+    ref = O.rmsnorm_gate(sh_o, y, np32(g), gamma, eps=1e-6)
+    got = np32(out)
+    scale = np.abs(ref) + 1e-30
+    # fp32: a few ulps; bf16: half an ulp of the 8-bit mantissa plus the fp32 error.
+    tol = 2e-6 if out_dtype == 0 else 2.0 ** -8 + 2e-6
+    assert np.max(np.abs(got - ref) / np.maximum(scale, 1e-3 * np.max(np.abs(ref)))) < tol
+    # gamma omitted == gamma of ones.
+    ones = torch.ones(H, dv, device=DEV)
+    a = sdm.sdm_rmsnorm_gate(sh_g, torch.from_numpy(y).to(DEV), g.to(DEV), None, out_dtype=out_dtype)
+    b = sdm.sdm_rmsnorm_gate(sh_g, torch.from_numpy(y).to(DEV), g.to(DEV), ones, out_dtype=out_dtype)
+    assert torch.equal(a, b)
+
+
+def test_forward_then_epilogue_matches_oracle():
+    w = WORKLOADS["gdn_matched"].with_(B=1, H=2, T=120)
+    x = generate(w)
+    sh_g, sh_o = gshape(w, sdm), oshape(w)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    gate = torch.sigmoid(torch.randn(w.B, w.H, w.T, w.d_v, generator=torch.Generator().manual_seed(3))).to(torch.bfloat16)
+    M = g["M0"].clone()
+    out = sdm.sdm_forward(sh_g, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M)
+    o = sdm.sdm_rmsnorm_gate(sh_g, out["y"], gate.to(DEV), out_dtype=sdm.SDM_F32)
+    status_ok()
+    ref = O.forward(sh_o, *(np32(x[k]) for k in ("q_w", "q_r", "K", "alpha", "beta", "v")),
+                    x["M0"].numpy())
+    if np.array_equal(out["idx_w"].cpu().numpy(), ref["idx_w"]) and \
+            np.array_equal(out["idx_r"].cpu().numpy(), ref["idx_r"]):
+        ro = O.rmsnorm_gate(sh_o, ref["y"], np32(gate), eps=1e-6)
+        assert max_rel(np32(o), ro) <= FTOL

@@ -204,6 +204,32 @@ sdm_status sdm_rmsnorm_gate(const sdm_shape* shape, const float* y, const void* 
                             const float* gamma, float eps, void* out,
                             sdm_dtype out_dtype, void* stream);
 
+/* Optional epilogue of sdm_decode: the arguments of sdm_rmsnorm_gate. */
+typedef struct {
+  const void* g;         /* [B,H,T,d_v] output gate, in shape->in_dtype      */
+  const float* gamma;    /* [H,d_v] per-head scale, or NULL for ones         */
+  float eps;             /* > 0                                              */
+  void* out;             /* [B,H,T,d_v] in out_dtype                         */
+  sdm_dtype out_dtype;   /* SDM_BF16 or SDM_F32                              */
+} sdm_epilogue;
+
+/* The forward step fused into one launch for short sequences -- decode,
+ * T = 1 per call [SDM notes 2.3-2.5; section 3 reports decode speed at the
+ * shapes of 2.8: sqrt N = 240 / 480, d_v = 960 / 1920].  Same arguments and
+ * results as sdm_forward (y, M in place, selections in idx_w/wt_w/idx_r/wt_r)
+ * plus, when `epi` is non-NULL, the sdm_rmsnorm_gate epilogue on y written
+ * to epi->out.  One CTA per (b,h) chain runs that chain's T steps in order,
+ * so the latency of a step is one chain's dependent path; use sdm_forward
+ * for long T.  Needs no workspace.  Sub-scores are fp32 FFMA for both
+ * input dtypes, so a selection can differ from one made on sdm_forward's
+ * tensor-core scores only where two candidate sums are within fp32 rounding
+ * of each other. */
+sdm_status sdm_decode(const sdm_shape* shape, const void* q_w, const void* q_r,
+                      const void* K, const void* alpha, const void* beta,
+                      const void* v, float* M, float* y, int32_t* idx_w,
+                      float* wt_w, int32_t* idx_r, float* wt_r,
+                      const sdm_epilogue* epi, void* stream);
+
 /* One full forward step: sdm_address then sdm_scan on `stream`.
  * Inputs as above; M updated in place, y written, and the selected indices
  * and weights returned in the caller's idx_w/wt_w/idx_r/wt_r buffers. */

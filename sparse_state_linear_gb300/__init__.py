@@ -26,7 +26,8 @@ STATUS = {0: "SDM_OK", 1: "SDM_ERR_INVALID_ARG", 2: "SDM_ERR_UNSUPPORTED", 3: "S
 
 EXPORTS = ["sdm_status_string", "sdm_subscores", "sdm_select", "sdm_address",
            "sdm_workspace_size", "sdm_scan", "sdm_scan_noalloc", "sdm_scan_logged",
-           "sdm_undo_workspace_size", "sdm_scan_undo", "sdm_rmsnorm_gate", "sdm_forward",
+           "sdm_undo_workspace_size", "sdm_scan_undo", "sdm_rmsnorm_gate", "sdm_decode",
+           "sdm_forward",
            "sdm_get_device_status",
            "sdm_set_scan_tuning", "sdm_selftest_wait_timeout"]
 
@@ -55,6 +56,12 @@ class Shape(ctypes.Structure):
 
     def __repr__(self):
         return "Shape(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+class Epilogue(ctypes.Structure):
+    """Mirror of ``sdm_epilogue`` in include/sdm.h."""
+    _fields_ = [("g", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("eps", ctypes.c_float),
+                ("out", ctypes.c_void_p), ("out_dtype", ctypes.c_int)]
 
 
 def make_shape(B, H, T, n_sub, d_h, d_v, W, R, k_w=0, k_r=0, in_dtype=SDM_BF16,
@@ -90,6 +97,7 @@ def lib():
         "sdm_undo_workspace_size": ([SP], ctypes.c_size_t),
         "sdm_scan_undo": ([SP, P, P, P, P, ctypes.c_size_t, P], I),
         "sdm_rmsnorm_gate": ([SP, P, P, P, ctypes.c_float, P, I, P], I),
+        "sdm_decode": ([SP] + [P] * 12 + [ctypes.POINTER(Epilogue), P], I),
         "sdm_forward": ([SP] + [P] * 13 + [ctypes.c_size_t, P], I),
         "sdm_get_device_status": ([P], I),
         "sdm_set_scan_tuning": ([I, I], I),
@@ -276,6 +284,34 @@ def sdm_rmsnorm_gate(sh: Shape, y, g, gamma=None, eps: float = 1e-6, out=None,
                                float(eps), _ptr(out, "out", (tdt,)), int(out_dtype),
                                _stream(stream)), "sdm_rmsnorm_gate")
     return out
+
+
+def sdm_decode(sh: Shape, q_w, q_r, K, alpha, beta, v, M, y=None, idx_w=None, wt_w=None,
+               idx_r=None, wt_r=None, gate=None, gamma=None, eps: float = 1e-6, out=None,
+               out_dtype=SDM_BF16, stream=None):
+    """Fused forward for short sequences (decode); M updated in place.  With a
+    gate, also the RMS-Norm + gate epilogue.  Returns dict(y, idx_w, wt_w,
+    idx_r, wt_r, out)."""
+    if y is None:
+        y = _empty((sh.B, sh.H, sh.T, sh.d_v), torch.float32, M)
+    idx_w, wt_w, idx_r, wt_r = _sel_outputs(sh, M, idx_w, wt_w, idx_r, wt_r)
+    dt, f32, i32 = _in_dt(sh), (torch.float32,), (torch.int32,)
+    epi = None
+    if gate is not None:
+        tdt = torch.bfloat16 if out_dtype == SDM_BF16 else torch.float32
+        if out is None:
+            out = _empty((sh.B, sh.H, sh.T, sh.d_v), tdt, M)
+        epi = Epilogue(_ptr(gate, "gate", dt).value,
+                       None if gamma is None else _ptr(gamma, "gamma", f32).value,
+                       float(eps), _ptr(out, "out", (tdt,)).value, int(out_dtype))
+    _ok(lib().sdm_decode(ctypes.byref(sh), _ptr(q_w, "q_w", dt), _ptr(q_r, "q_r", dt),
+                         _ptr(K, "K", dt), _ptr(alpha, "alpha", dt), _ptr(beta, "beta", dt),
+                         _ptr(v, "v", dt), _ptr(M, "M", f32), _ptr(y, "y", f32),
+                         _ptr(idx_w, "idx_w", i32), _ptr(wt_w, "wt_w", f32),
+                         _ptr(idx_r, "idx_r", i32), _ptr(wt_r, "wt_r", f32),
+                         None if epi is None else ctypes.byref(epi), _stream(stream)),
+        "sdm_decode")
+    return dict(y=y, idx_w=idx_w, wt_w=wt_w, idx_r=idx_r, wt_r=wt_r, out=out)
 
 
 def sdm_forward(sh: Shape, q_w, q_r, K, alpha, beta, v, M, y=None, idx_w=None, wt_w=None,

@@ -1,0 +1,355 @@
+// decode.cu -- one fused launch for short sequences (decode, T = 1).
+//
+// [SDM notes] "Sparse Delta Memory：中文精读笔记": 2.3 (product-key addressing),
+// 2.4 Eq. (3)-(5) (gated delta write, read after the write; after Eq. (5) the
+// per-head RMS-Norm and output gate), 2.5 (the Fig. 2 shared-residual form).
+// The notes' section 3 reports decode speed as the inference number, and
+// 2.8 gives the per-head shapes it runs at (sqrt N = 240 / 480, d_v = 960 /
+// 1920 with 2 heads).
+//
+// A decode step has little work per chain but a long dependent path
+// (scores -> top-k -> merge -> write -> read), so the tile kernels used for
+// long sequences spend most of it waiting.  Here one CTA owns one (b, h)
+// chain and runs its T steps in order, each step entirely on chip:
+//   scores    FFMA (or inverse distance) of the four half-queries against
+//             the two sub-key tables, into shared memory;
+//   top-k     warps 0-3, one half-row each (select.cuh, exact);
+//   merge     warps 0-1, staircase merge + softmax (select.cuh);
+//   write     every thread owns 16-byte column chunks of the row and walks
+//             the W write rows in register batches, so the row loads of a
+//             batch are in flight together; Fig. 2 form: a first pass sums
+//             the shared prediction, a second writes;
+//   read      after a block barrier (the CTA's own global writes are then
+//             visible to all its threads) the R read rows, batched the same
+//             way; optionally the RMS-Norm + gate epilogue, whose row sum of
+//             squares is a block reduction because the whole row is here.
+// The table is read with plain (coherent) loads: the CTA rewrites it.
+#include "common.cuh"
+#include "internal.h"
+#include "select.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kStairCap = 320;   // >= sum_{a<64} floor(64/(a+1)) = 280
+constexpr int kBatch = 8;        // table rows in flight per thread
+
+struct DecArgs {
+  Dims d;
+  const void* q_w;
+  const void* q_r;
+  const void* K;
+  const void* alpha;
+  const void* beta;
+  const void* v;
+  float* M;
+  float* y;
+  int32_t* idx_w;
+  float* wt_w;
+  int32_t* idx_r;
+  float* wt_r;
+  const void* g;        // epilogue gate [B,H,T,d_v] (in_dtype) or null
+  const float* gamma;   // [H,d_v] or null
+  void* out;            // epilogue output or null (no epilogue)
+  float eps;
+  int out_dtype;
+};
+
+struct DecLayout {
+  size_t q, S, lv, lid, ws, stair, nst, sel, red, total;
+};
+
+__host__ __device__ inline size_t dl_align(size_t x) { return (x + 15) / 16 * 16; }
+
+__host__ __device__ inline DecLayout dec_layout(int s, int dh) {
+  DecLayout L;
+  size_t o = 0;
+  L.q = o;     o = dl_align(o + sizeof(float) * 4 * (size_t)dh);
+  L.S = o;     o = dl_align(o + sizeof(float) * 4 * (size_t)s);
+  L.lv = o;    o = dl_align(o + sizeof(float) * 4 * kMaxSel);
+  L.lid = o;   o = dl_align(o + sizeof(uint32_t) * 4 * kMaxSel);
+  L.ws = o;    o = dl_align(o + sizeof(WarpScratch) * 4);
+  L.stair = o; o = dl_align(o + sizeof(uint16_t) * 2 * kStairCap);
+  L.nst = o;   o = dl_align(o + sizeof(int) * 2);
+  L.sel = o;   o = dl_align(o + sizeof(float) * 4 * kMaxSel);   // idx_w, wt_w, idx_r, wt_r
+  L.red = o;   o = dl_align(o + sizeof(float) * kDecWarps);
+  L.total = o;
+  return L;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float4 ld_in4(const void* base, size_t i4) {
+  if (BF16) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(base) + i4);
+    return make_float4(bf16_bits_to_float(w.x & 0xffffu), bf16_bits_to_float(w.x >> 16),
+                       bf16_bits_to_float(w.y & 0xffffu), bf16_bits_to_float(w.y >> 16));
+  }
+  return __ldg(reinterpret_cast<const float4*>(base) + i4);
+}
+
+__device__ __forceinline__ void st_out4(void* base, size_t i4, int dt, float4 v) {
+  if (dt == SDM_F32) {
+    reinterpret_cast<float4*>(base)[i4] = v;
+    return;
+  }
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&a);
+  w.y = *reinterpret_cast<const uint32_t*>(&b);
+  reinterpret_cast<uint2*>(base)[i4] = w;
+}
+
+// Element e of a dh-long input vector (bf16 or fp32) as float.
+template <bool BF16>
+__device__ __forceinline__ float ld_in1(const void* base, size_t e) {
+  if (BF16) return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(base) + e));
+  return __ldg(reinterpret_cast<const float*>(base) + e);
+}
+
+template <int PL, bool BF16, int KIND>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const Dims& d = A.d;
+  const DecLayout L = dec_layout(d.s, d.dh);
+  float* qs = reinterpret_cast<float*>(smem + L.q);
+  float* S = reinterpret_cast<float*>(smem + L.S);
+  float* lv = reinterpret_cast<float*>(smem + L.lv);
+  uint32_t* lid = reinterpret_cast<uint32_t*>(smem + L.lid);
+  WarpScratch* wsa = reinterpret_cast<WarpScratch*>(smem + L.ws);
+  uint16_t* stair = reinterpret_cast<uint16_t*>(smem + L.stair);
+  int* nst = reinterpret_cast<int*>(smem + L.nst);
+  int32_t* sidx = reinterpret_cast<int32_t*>(smem + L.sel);      // [2][64]
+  float* swt = reinterpret_cast<float*>(smem + L.sel) + 2 * kMaxSel;
+  float* red = reinterpret_cast<float*>(smem + L.red);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chain = blockIdx.x;              // b * H + h
+  const int h = chain % d.H;
+  const int s = d.s, dh = d.dh, dv = d.dv, W = d.W, R = d.R;
+  const int nc4 = dv / 4;
+  float* Mc = A.M + (size_t)chain * (size_t)d.N() * dv;
+  const bool fig2 = d.update == SDM_UPDATE_SHARED_RESIDUAL;
+
+  if (warp == 2) {
+    const int n = build_stair(W, d.kw, stair, lane);
+    if (lane == 0) nst[0] = n;
+  } else if (warp == 3) {
+    const int n = build_stair(R, d.kr, stair + kStairCap, lane);
+    if (lane == 0) nst[1] = n;
+  }
+
+  for (int t = 0; t < d.T; ++t) {
+    const size_t th = (size_t)chain * d.T + t;
+    // ---- half-queries: qs[(sigma * 2 + p) * dh + c]
+    for (int e = tid; e < 4 * dh; e += kDecThreads) {
+      const int sg = e / (2 * dh), rem = e - sg * 2 * dh;
+      qs[e] = ld_in1<BF16>(sg == 0 ? A.q_w : A.q_r, th * 2 * dh + rem);
+    }
+    __syncthreads();
+    // ---- sub-scores S[(sigma * 2 + p) * s + j]
+    for (int e = tid; e < 4 * s; e += kDecThreads) {
+      const int row = e / s, j = e - row * s;
+      const int p = row & 1;
+      const float* q = qs + row * dh;
+      const size_t kb = ((size_t)(h * 2 + p) * s + j) * dh;
+      float acc = 0.f;
+      for (int c = 0; c < dh; c += 4) {
+        const float4 k4 = ld_in4<BF16>(A.K, (kb + c) / 4);
+        if (KIND == SDM_SCORE_DOT) {
+          acc = fmaf(q[c], k4.x, acc);
+          acc = fmaf(q[c + 1], k4.y, acc);
+          acc = fmaf(q[c + 2], k4.z, acc);
+          acc = fmaf(q[c + 3], k4.w, acc);
+        } else {
+          float df;
+          df = q[c] - k4.x;     acc = fmaf(df, df, acc);
+          df = q[c + 1] - k4.y; acc = fmaf(df, df, acc);
+          df = q[c + 2] - k4.z; acc = fmaf(df, df, acc);
+          df = q[c + 3] - k4.w; acc = fmaf(df, df, acc);
+        }
+      }
+      S[e] = KIND == SDM_SCORE_DOT ? acc : -logf(d.eps + acc);
+    }
+    __syncthreads();
+    // ---- per-half top-k: warp w < 4 takes half-row w = sigma * 2 + p
+    if (warp < 4) {
+      const int k = (warp >> 1) == 0 ? d.kw : d.kr;
+      WarpScratch& ws = wsa[warp];
+      RowSrc src{S + warp * s};
+      warp_topk<PL>(src, s, k, ws, lane);
+      for (int e = lane; e < k; e += 32) {
+        lv[warp * kMaxSel + e] = ws.out_v[e];
+        lid[warp * kMaxSel + e] = ws.out_id[e];
+      }
+    }
+    __syncthreads();
+    // ---- merge + softmax: warp sigma < 2
+    if (warp < 2) {
+      const int sg = warp;
+      const int k = sg == 0 ? d.kw : d.kr, nsel = sg == 0 ? W : R;
+      WarpScratch& ws = wsa[sg];
+      warp_merge(lv + (2 * sg) * kMaxSel, lid + (2 * sg) * kMaxSel, lv + (2 * sg + 1) * kMaxSel,
+                 lid + (2 * sg + 1) * kMaxSel, k, nsel, (uint32_t)s, stair + sg * kStairCap,
+                 nst[sg], ws, lane);
+      warp_softmax_store(ws, nsel, sidx + sg * kMaxSel, swt + sg * kMaxSel, lane);
+      __syncwarp();
+      int32_t* io = (sg == 0 ? A.idx_w : A.idx_r) + th * nsel;
+      float* wo = (sg == 0 ? A.wt_w : A.wt_r) + th * nsel;
+      for (int e = lane; e < nsel; e += 32) {
+        io[e] = sidx[sg * kMaxSel + e];
+        wo[e] = swt[sg * kMaxSel + e];
+      }
+    }
+    __syncthreads();
+
+    // ---- write (Eq. (3)-(4), or the Fig. 2 form)
+    const float a = load_scalar(A.alpha, th, d.in_dtype);
+    const float bt = load_scalar(A.beta, th, d.in_dtype);
+    for (int c4 = tid; c4 < nc4; c4 += kDecThreads) {
+      const float4 vv = ld_in4<BF16>(A.v, th * nc4 + c4);
+      float4 res = vv;
+      if (fig2) {
+        float4 vh = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = 0; j0 < W; j0 += kBatch) {
+          float4 x[kBatch];
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u)
+            if (j0 + u < W)
+              x[u] = reinterpret_cast<const float4*>(Mc + (size_t)sidx[j0 + u] * dv)[c4];
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u)
+            if (j0 + u < W) {
+              const float wj = swt[j0 + u];
+              vh.x = fmaf(wj, a * x[u].x, vh.x);
+              vh.y = fmaf(wj, a * x[u].y, vh.y);
+              vh.z = fmaf(wj, a * x[u].z, vh.z);
+              vh.w = fmaf(wj, a * x[u].w, vh.w);
+            }
+        }
+        res = make_float4(vv.x - vh.x, vv.y - vh.y, vv.z - vh.z, vv.w - vh.w);
+      }
+      for (int j0 = 0; j0 < W; j0 += kBatch) {
+        float4 x[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (j0 + u < W) x[u] = reinterpret_cast<const float4*>(Mc + (size_t)sidx[j0 + u] * dv)[c4];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (j0 + u < W) {
+            const float cw = bt * swt[j0 + u];
+            float4 o;
+            float m;
+            if (fig2) {
+              m = a * x[u].x; o.x = fmaf(cw, res.x, m);
+              m = a * x[u].y; o.y = fmaf(cw, res.y, m);
+              m = a * x[u].z; o.z = fmaf(cw, res.z, m);
+              m = a * x[u].w; o.w = fmaf(cw, res.w, m);
+            } else {
+              m = a * x[u].x; o.x = fmaf(cw, vv.x - m, m);
+              m = a * x[u].y; o.y = fmaf(cw, vv.y - m, m);
+              m = a * x[u].z; o.z = fmaf(cw, vv.z - m, m);
+              m = a * x[u].w; o.w = fmaf(cw, vv.w - m, m);
+            }
+            reinterpret_cast<float4*>(Mc + (size_t)sidx[j0 + u] * dv)[c4] = o;
+          }
+      }
+    }
+    __syncthreads();
+
+    // ---- read after the write (Eq. (5)), then the optional epilogue
+    constexpr int kMaxC = 2;                 // d_v <= 2048: at most 2 chunks per thread
+    float4 yv[kMaxC];
+    float ss = 0.f;
+#pragma unroll
+    for (int ci = 0; ci < kMaxC; ++ci) {
+      const int c4 = tid + ci * kDecThreads;
+      yv[ci] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c4 >= nc4) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q0 = 0; q0 < R; q0 += kBatch) {
+        float4 x[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (q0 + u < R)
+            x[u] = reinterpret_cast<const float4*>(Mc + (size_t)sidx[kMaxSel + q0 + u] * dv)[c4];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (q0 + u < R) {
+            const float w = swt[kMaxSel + q0 + u];
+            acc.x = fmaf(w, x[u].x, acc.x);
+            acc.y = fmaf(w, x[u].y, acc.y);
+            acc.z = fmaf(w, x[u].z, acc.z);
+            acc.w = fmaf(w, x[u].w, acc.w);
+          }
+      }
+      reinterpret_cast<float4*>(A.y + th * dv)[c4] = acc;
+      yv[ci] = acc;
+      ss = fmaf(acc.x, acc.x, ss);
+      ss = fmaf(acc.y, acc.y, ss);
+      ss = fmaf(acc.z, acc.z, ss);
+      ss = fmaf(acc.w, acc.w, ss);
+    }
+    if (A.out) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      if (lane == 0) red[warp] = ss;
+      __syncthreads();
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) tot += red[w];
+      const float inv = 1.f / sqrtf(tot / (float)dv + A.eps);
+#pragma unroll
+      for (int ci = 0; ci < kMaxC; ++ci) {
+        const int c4 = tid + ci * kDecThreads;
+        if (c4 >= nc4) continue;
+        const float4 gt = ld_in4<BF16>(A.g, th * nc4 + c4);
+        const float4 sc = A.gamma ? __ldg(reinterpret_cast<const float4*>(A.gamma) +
+                                          (size_t)h * nc4 + c4)
+                                  : make_float4(1.f, 1.f, 1.f, 1.f);
+        st_out4(A.out, th * nc4 + c4, A.out_dtype,
+                make_float4(yv[ci].x * inv * sc.x * gt.x, yv[ci].y * inv * sc.y * gt.y,
+                            yv[ci].z * inv * sc.z * gt.z, yv[ci].w * inv * sc.w * gt.w));
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <int PL, bool BF16, int KIND>
+cudaError_t launch_dec(const DecArgs& A, cudaStream_t stream) {
+  const size_t smem = dec_layout(A.d.s, A.d.dh).total;
+  auto kfn = decode_kernel<PL, BF16, KIND>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kfn<<<(unsigned)(A.d.B * A.d.H), kDecThreads, smem, stream>>>(A);
+  return cudaGetLastError();
+}
+
+template <int PL>
+cudaError_t launch_pl(const DecArgs& A, cudaStream_t stream) {
+  const bool bf = A.d.in_dtype == SDM_BF16;
+  if (A.d.score == SDM_SCORE_DOT)
+    return bf ? launch_dec<PL, true, SDM_SCORE_DOT>(A, stream)
+              : launch_dec<PL, false, SDM_SCORE_DOT>(A, stream);
+  return bf ? launch_dec<PL, true, SDM_SCORE_IDW>(A, stream)
+            : launch_dec<PL, false, SDM_SCORE_IDW>(A, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const Dims& d, const void* q_w, const void* q_r, const void* K,
+                          const void* alpha, const void* beta, const void* v, float* M, float* y,
+                          int32_t* idx_w, float* wt_w, int32_t* idx_r, float* wt_r,
+                          const void* g, const float* gamma, float eps, void* out,
+                          int out_dtype, cudaStream_t stream) {
+  if ((long long)d.B * d.H == 0 || d.T == 0) return cudaSuccess;
+  DecArgs A{d, q_w, q_r, K, alpha, beta, v, M, y, idx_w, wt_w, idx_r, wt_r,
+            g, gamma, out, eps, out_dtype};
+  return d.s <= 256 ? launch_pl<8>(A, stream) : launch_pl<16>(A, stream);
+}
+
+}  // namespace sdm

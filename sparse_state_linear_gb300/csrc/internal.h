@@ -53,6 +53,14 @@ cudaError_t launch_undo(const Dims& d, const int32_t* idx_w, const float* undo, 
 cudaError_t launch_rmsnorm_gate(const Dims& d, const float* y, const void* g, const float* gamma,
                                 float eps, void* out, int out_dtype, cudaStream_t stream);
 
+// Fused decode (decode.cu): one CTA per (b,h) chain runs its T steps --
+// addressing, write, read and, when out is non-null, the epilogue.
+cudaError_t launch_decode(const Dims& d, const void* q_w, const void* q_r, const void* K,
+                          const void* alpha, const void* beta, const void* v, float* M, float* y,
+                          int32_t* idx_w, float* wt_w, int32_t* idx_r, float* wt_r,
+                          const void* g, const float* gamma, float eps, void* out,
+                          int out_dtype, cudaStream_t stream);
+
 // Accessors of the API layer (sdm_api.cu) for other entry points.
 sdm_status api_check_shape(const sdm_shape* shape, Dims* d);
 sdm_status api_status_ptr(unsigned** out);

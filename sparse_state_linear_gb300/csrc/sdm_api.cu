@@ -300,6 +300,42 @@ sdm_status sdm_rmsnorm_gate(const sdm_shape* shape, const float* y, const void* 
                                        static_cast<cudaStream_t>(stream)));
 }
 
+sdm_status sdm_decode(const sdm_shape* shape, const void* q_w, const void* q_r, const void* K,
+                      const void* alpha, const void* beta, const void* v, float* M, float* y,
+                      int32_t* idx_w, float* wt_w, int32_t* idx_r, float* wt_r,
+                      const sdm_epilogue* epi, void* stream) {
+  Dims d;
+  sdm_status st = check_shape(shape, &d);
+  if (st != SDM_OK) return st;
+  if (epi) {
+    if (!(epi->eps > 0.f) || !(epi->eps < INFINITY)) return SDM_ERR_INVALID_ARG;
+    if (epi->out_dtype != SDM_F32 && epi->out_dtype != SDM_BF16) return SDM_ERR_INVALID_ARG;
+  }
+  if (empty_work(d)) return SDM_OK;   // no work: pointers are not looked at
+  SDM_CHECK_PTR(q_w);
+  SDM_CHECK_PTR(q_r);
+  SDM_CHECK_PTR(K);
+  SDM_CHECK_PTR(alpha);
+  SDM_CHECK_PTR(beta);
+  SDM_CHECK_PTR(v);
+  SDM_CHECK_PTR(M);
+  SDM_CHECK_PTR(y);
+  SDM_CHECK_PTR(idx_w);
+  SDM_CHECK_PTR(wt_w);
+  SDM_CHECK_PTR(idx_r);
+  SDM_CHECK_PTR(wt_r);
+  if (epi) {
+    SDM_CHECK_PTR(epi->g);
+    SDM_CHECK_PTR(epi->out);
+    if (epi->gamma && !aligned16(epi->gamma)) return SDM_ERR_INVALID_ARG;
+  }
+  return from_cuda(launch_decode(d, q_w, q_r, K, alpha, beta, v, M, y, idx_w, wt_w, idx_r,
+                                 wt_r, epi ? epi->g : nullptr, epi ? epi->gamma : nullptr,
+                                 epi ? epi->eps : 0.f, epi ? epi->out : nullptr,
+                                 epi ? (int)epi->out_dtype : 0,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
 sdm_status sdm_get_device_status(void* stream) {
   unsigned* sp = nullptr;
   sdm_status st = status_ptr(&sp);

@@ -546,3 +546,118 @@ def test_forward_then_epilogue_matches_oracle():
             np.array_equal(out["idx_r"].cpu().numpy(), ref["idx_r"]):
         ro = O.rmsnorm_gate(sh_o, ref["y"], np32(gate), eps=1e-6)
         assert max_rel(np32(o), ro) <= FTOL
+
+
+# ------------------------------------------------------------------ decode
+
+def compact_oracle_scan(idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0_dev, update_form):
+    """The oracle scan of a short segment on a compact table that holds only
+    the rows the segment touches (exact: no other row is ever read)."""
+    B, H, T, W = idx_w.shape
+    R = idx_r.shape[-1]
+    dv = M0_dev.shape[-1]
+    rows = [[np.unique(np.concatenate([idx_w[b, h].ravel(), idx_r[b, h].ravel()]))
+             for h in range(H)] for b in range(B)]
+    n = max(len(r) for rr in rows for r in rr)
+    s2 = int(np.ceil(np.sqrt(n)))
+    Mc = np.zeros((B, H, s2 * s2, dv), np.float32)
+    iw, ir = np.empty_like(idx_w), np.empty_like(idx_r)
+    for b in range(B):
+        for h in range(H):
+            r = rows[b][h]
+            Mc[b, h, :len(r)] = M0_dev[b, h, torch.from_numpy(r).long().to(DEV)].cpu().numpy()
+            iw[b, h] = np.searchsorted(r, idx_w[b, h])
+            ir[b, h] = np.searchsorted(r, idx_r[b, h])
+    sh = O.Shape(B=B, H=H, T=T, n_sub=s2, d_h=16, d_v=dv, W=W, R=R, update_form=update_form)
+    Mo, yo = O.scan(sh, iw, wt_w, ir, wt_r, alpha, beta, v, Mc)
+    return rows, Mo, yo
+
+
+DECODE_CASES = [  # B, H, T, s, d_h, d_v, W, R, bf16, score, form
+    (3, 2, 1, 32, 16, 32, 8, 8, False, 0, 0),
+    (2, 2, 1, 128, 64, 128, 64, 64, True, 0, 0),
+    (2, 2, 1, 240, 64, 960, 64, 64, True, 0, 0),      # 1.4B-scale head
+    (1, 2, 1, 480, 64, 1920, 64, 64, True, 0, 0),     # 8B-scale head
+    (1, 1, 2, 512, 256, 512, 8, 8, False, 1, 0),      # inverse-distance scores
+    (2, 1, 3, 8, 16, 64, 16, 16, False, 0, 0),        # rows reused across steps
+    (2, 2, 1, 240, 64, 960, 64, 64, True, 0, 1),      # Fig. 2 form
+    (2, 1, 3, 8, 16, 64, 16, 16, True, 0, 1),
+]
+
+
+@pytest.mark.parametrize("case", DECODE_CASES, ids=lambda c: "B{}H{}T{}s{}dv{}W{}f{}{}".format(
+    c[0], c[1], c[2], c[3], c[5], c[6], c[10], "idw" if c[9] else ""))
+@pytest.mark.parametrize("epi", [False, True])
+def test_decode_matches_oracle(case, epi):
+    B, H, T, s, dh, dv, W, R, bf16, score, form = case
+    w = WORKLOADS["mid"].with_(B=B, H=H, T=T, n_sub=s, d_h=dh, d_v=16, W=W, R=R, bf16=bf16,
+                               score_kind=score, update_form=form,
+                               qk_std=1.0 if score else WORKLOADS["mid"].qk_std)
+    x = generate(w)                                   # q, K, gates (v, M0 drawn below)
+    gen = torch.Generator(device=DEV).manual_seed(s + dv)
+    dt = torch.bfloat16 if bf16 else torch.float32
+    v = torch.randn(B, H, T, dv, generator=gen, device=DEV).to(dt)
+    M0 = torch.randn(B, H, s * s, dv, generator=gen, device=DEV) * 0.02
+    sh_g = sdm.make_shape(B, H, T, s, dh, dv, W, R, in_dtype=sdm.SDM_BF16 if bf16 else sdm.SDM_F32,
+                          score=score, update=form)
+    g = {k: t.to(DEV) for k, t in x.items() if k in ("q_w", "q_r", "K", "alpha", "beta")}
+    M = M0.clone()
+    gate = gamma = None
+    if epi:
+        gate = torch.sigmoid(torch.randn(B, H, T, dv, generator=gen, device=DEV)).to(dt)
+        gamma = torch.rand(H, dv, generator=gen, device=DEV) + 0.5
+    out = sdm.sdm_decode(sh_g, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], v, M,
+                         gate=gate, gamma=gamma, out_dtype=sdm.SDM_F32)
+    status_ok()
+    sh_o = O.Shape(B=B, H=H, T=T, n_sub=s, d_h=dh, d_v=dv, W=W, R=R, score_kind=score,
+                   idw_eps=w.idw_eps, update_form=form)
+    S_w = O.subscores(sh_o, np32(x["q_w"]), np32(x["K"]))
+    S_r = O.subscores(sh_o, np32(x["q_r"]), np32(x["K"]))
+    ow, orr = O.select(sh_o, 0, S_w), O.select(sh_o, 1, S_r)
+    iw, ir = out["idx_w"].cpu().numpy(), out["idx_r"].cpu().numpy()
+    check_indices(iw, ow[0], S_w, s)
+    check_indices(ir, orr[0], S_r, s)
+    ww, wr = np32(out["wt_w"]).astype(np.float64), np32(out["wt_r"]).astype(np.float64)
+    same = np.all(iw == ow[0], axis=-1) & np.all(ir == orr[0], axis=-1)
+    assert np.max(np.abs(ww[same] - ow[2][same]), initial=0) < 1e-5
+    # The scan part, on the device's own selections.
+    rows, Mo, yo = compact_oracle_scan(iw, ww, ir, wr, np32(x["alpha"]), np32(x["beta"]),
+                                       np32(v), M0, form)
+    assert max_rel(np32(out["y"]), yo) <= FTOL
+    Mg = M.cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            r = rows[b][h]
+            assert max_rel(Mg[b, h, r], Mo[b, h, :len(r)]) <= FTOL
+    # Only the touched rows changed.
+    changed = (M != M0).any(dim=-1).cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            assert set(np.nonzero(changed[b, h])[0].tolist()) <= set(iw[b, h].ravel().tolist())
+    if epi:
+        ref = O.rmsnorm_gate(sh_o, yo, np32(gate), np32(gamma), eps=1e-6)
+        assert max_rel(np32(out["out"]), ref) <= FTOL
+
+
+def test_decode_agrees_with_forward():
+    """Device vs device at the 1.4B-scale head: same selections wherever the
+    two score paths agree, and then the same results."""
+    B, H, s, dh, dv = 8, 2, 240, 64, 960
+    gen = torch.Generator(device=DEV).manual_seed(7)
+    q_w = (torch.randn(B, H, 1, 2, dh, generator=gen, device=DEV) / 4).bfloat16()
+    q_r = (torch.randn(B, H, 1, 2, dh, generator=gen, device=DEV) / 4).bfloat16()
+    K = (torch.randn(H, 2, s, dh, generator=gen, device=DEV) / 4).bfloat16()
+    v = torch.randn(B, H, 1, dv, generator=gen, device=DEV).bfloat16()
+    alpha = (0.9 + 0.1 * torch.rand(B, H, 1, generator=gen, device=DEV)).bfloat16()
+    beta = torch.rand(B, H, 1, generator=gen, device=DEV).bfloat16()
+    M0 = torch.randn(B, H, s * s, dv, generator=gen, device=DEV) * 0.02
+    sh = sdm.make_shape(B, H, 1, s, dh, dv, 64, 64)
+    M1, M2 = M0.clone(), M0.clone()
+    a = sdm.sdm_decode(sh, q_w, q_r, K, alpha, beta, v, M1)
+    b = sdm.sdm_forward(sh, q_w, q_r, K, alpha, beta, v, M2)
+    status_ok()
+    same = (torch.all(a["idx_w"] == b["idx_w"], -1) & torch.all(a["idx_r"] == b["idx_r"], -1))
+    assert same.float().mean() > 0.9
+    ya, yb = np32(a["y"]), np32(b["y"])
+    sm = same.cpu().numpy()
+    assert max_rel(ya[sm], yb[sm]) <= FTOL

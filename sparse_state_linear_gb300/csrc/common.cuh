@@ -52,6 +52,11 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
                : "memory");
 }
 
+// Ask L2 to fetch the 128-byte line holding `p` (no register, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
                : "memory");

@@ -34,7 +34,7 @@ namespace {
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kStairCap = 320;   // >= sum_{a<64} floor(64/(a+1)) = 280
-constexpr int kBatch = 8;        // table rows in flight per thread
+constexpr int kBatch = 16;       // table rows in flight per thread
 
 struct DecArgs {
   Dims d;
@@ -102,6 +102,34 @@ __device__ __forceinline__ void st_out4(void* base, size_t i4, int dt, float4 v)
   reinterpret_cast<uint2*>(base)[i4] = w;
 }
 
+// 16 consecutive input elements (bf16 or fp32) from element e (a multiple of
+// 16), all loads issued before any is used.
+template <bool BF16>
+__device__ __forceinline__ void ld_in16(const void* base, size_t e, float (&k)[16]) {
+  if (BF16) {
+    const uint4* p = reinterpret_cast<const uint4*>(base) + e / 8;
+    const uint4 a = __ldg(p), b = __ldg(p + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      k[2 * i] = bf16_bits_to_float(w[i] & 0xffffu);
+      k[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(base) + e / 4;
+    float4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __ldg(p + i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      k[4 * i] = v[i].x;
+      k[4 * i + 1] = v[i].y;
+      k[4 * i + 2] = v[i].z;
+      k[4 * i + 3] = v[i].w;
+    }
+  }
+}
+
 // Element e of a dh-long input vector (bf16 or fp32) as float.
 template <bool BF16>
 __device__ __forceinline__ float ld_in1(const void* base, size_t e) {
@@ -141,6 +169,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
     if (lane == 0) nst[1] = n;
   }
 
+  {
+    // The head's sub-key tables, line by line, into L2 for the first scores.
+    const size_t kbytes = (size_t)2 * s * dh * (BF16 ? 2 : 4);
+    const unsigned char* kb = static_cast<const unsigned char*>(A.K) + (size_t)h * kbytes;
+    for (size_t o = (size_t)tid * 128; o < kbytes; o += (size_t)kDecThreads * 128)
+      prefetch_l2(kb + o);
+  }
+
   for (int t = 0; t < d.T; ++t) {
     const size_t th = (size_t)chain * d.T + t;
     // ---- half-queries: qs[(sigma * 2 + p) * dh + c]
@@ -149,29 +185,33 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
       qs[e] = ld_in1<BF16>(sg == 0 ? A.q_w : A.q_r, th * 2 * dh + rem);
     }
     __syncthreads();
-    // ---- sub-scores S[(sigma * 2 + p) * s + j]
-    for (int e = tid; e < 4 * s; e += kDecThreads) {
-      const int row = e / s, j = e - row * s;
-      const int p = row & 1;
-      const float* q = qs + row * dh;
+    // ---- sub-scores S[(sigma * 2 + p) * s + j]: one thread per (p, j) loads
+    // sub-key K_p[j] once, 16 elements at a time with every load of a chunk
+    // in flight, and scores it against both branches' half-queries.
+    for (int e = tid; e < 2 * s; e += kDecThreads) {
+      const int p = e / s, j = e - p * s;
+      const float* qw = qs + p * dh;           // write branch, half p
+      const float* qr = qs + (2 + p) * dh;     // read branch, half p
       const size_t kb = ((size_t)(h * 2 + p) * s + j) * dh;
-      float acc = 0.f;
-      for (int c = 0; c < dh; c += 4) {
-        const float4 k4 = ld_in4<BF16>(A.K, (kb + c) / 4);
-        if (KIND == SDM_SCORE_DOT) {
-          acc = fmaf(q[c], k4.x, acc);
-          acc = fmaf(q[c + 1], k4.y, acc);
-          acc = fmaf(q[c + 2], k4.z, acc);
-          acc = fmaf(q[c + 3], k4.w, acc);
-        } else {
-          float df;
-          df = q[c] - k4.x;     acc = fmaf(df, df, acc);
-          df = q[c + 1] - k4.y; acc = fmaf(df, df, acc);
-          df = q[c + 2] - k4.z; acc = fmaf(df, df, acc);
-          df = q[c + 3] - k4.w; acc = fmaf(df, df, acc);
+      float aw = 0.f, ar = 0.f;
+#pragma unroll 2
+      for (int c0 = 0; c0 < dh; c0 += 16) {
+        float k[16];
+        ld_in16<BF16>(A.K, kb + c0, k);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (KIND == SDM_SCORE_DOT) {
+            aw = fmaf(qw[c0 + i], k[i], aw);
+            ar = fmaf(qr[c0 + i], k[i], ar);
+          } else {
+            const float dw = qw[c0 + i] - k[i], dr = qr[c0 + i] - k[i];
+            aw = fmaf(dw, dw, aw);
+            ar = fmaf(dr, dr, ar);
+          }
         }
       }
-      S[e] = KIND == SDM_SCORE_DOT ? acc : -logf(d.eps + acc);
+      S[p * s + j] = KIND == SDM_SCORE_DOT ? aw : -logf(d.eps + aw);
+      S[(2 + p) * s + j] = KIND == SDM_SCORE_DOT ? ar : -logf(d.eps + ar);
     }
     __syncthreads();
     // ---- per-half top-k: warp w < 4 takes half-row w = sigma * 2 + p

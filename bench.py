@@ -5,6 +5,7 @@ One step = one sdm_forward over one batch of the workload (default
 inputs, fp32 table of 2 GiB).  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--variant forward|fig2|logged|decode] [--workload NAME]
 
 --impl reference times the CPU oracle (the plain C++ restatement of the
 method) on this machine's host cores, on a bounded sample of the same workload.
@@ -156,7 +157,7 @@ def oracle_sample_rate(w, budget_s: float, seed_offset: int = 0):
     growing the token count until about `budget_s` seconds of work.  Returns
     (equivalent tokens/s of the whole workload, description)."""
     import oracle as O
-    T = 64
+    T = min(64, w.T)
     spent = 0.0
     last = None
     while True:
@@ -229,6 +230,16 @@ def config_of(w):
             "l2": f"inputs larger than L2 (fp32 table {w.B * w.H * w.N * w.d_v * 4 / 2**30:.2f} GiB)"}
 
 
+def variant_workload(args):
+    """The workload a --variant runs on (forward: --workload as given)."""
+    w = WORKLOADS[args.workload]
+    if args.variant == "fig2":
+        w = w.with_(update_form=1)
+    if args.variant == "decode" and w.T != 1:
+        w = WORKLOADS["decode_l08"]
+    return w
+
+
 def run_ours(args, w):
     import sparse_state_linear_gb300 as sdm
     ws, rank, local = dist_env()
@@ -239,7 +250,9 @@ def run_ours(args, w):
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     sdm.lib()
-    x = generate(rank_workload(w, rank))
+    rw = rank_workload(w, rank)
+    big = rw.B * rw.H * rw.N * rw.d_v * 4 > (8 << 30)
+    x = generate(rw, device=dev if big else None)
     g = {k: t.to(dev) for k, t in x.items() if k != "M0"}
     M = x["M0"].to(dev)
     del x
@@ -253,11 +266,34 @@ def run_ours(args, w):
     wt_w = torch.empty(BHT + (w.W,), dtype=torch.float32, device=dev)
     wt_r = torch.empty(BHT + (w.R,), dtype=torch.float32, device=dev)
     wsp = torch.empty(max(16, sdm.sdm_workspace_size(sh)), dtype=torch.uint8, device=dev)
+    undo = uws = None
+    if args.variant == "logged":
+        undo = torch.empty(BHT + (w.W, w.d_v), dtype=torch.float32, device=dev)
+        uws = torch.empty(max(16, sdm.sdm_undo_workspace_size(sh)), dtype=torch.uint8,
+                          device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    def address():
+        sdm.sdm_address(sh, g["q_w"], g["q_r"], g["K"], idx_w, wt_w, idx_r, wt_r, stream=stream)
+
+    def scan():
+        if undo is not None:
+            sdm.sdm_scan_logged(sh, idx_w, wt_w, idx_r, wt_r, g["alpha"], g["beta"], g["v"], M, y,
+                                undo=undo, workspace=wsp, stream=stream)
+        else:
+            sdm.sdm_scan(sh, idx_w, wt_w, idx_r, wt_r, g["alpha"], g["beta"], g["v"], M, y,
+                         workspace=wsp, stream=stream)
+
     def forward():
-        sdm.sdm_forward(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M, y,
-                        idx_w, wt_w, idx_r, wt_r, workspace=wsp, stream=stream)
+        if args.variant == "decode":
+            sdm.sdm_decode(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M, y,
+                           idx_w, wt_w, idx_r, wt_r, stream=stream)
+        elif undo is not None:
+            address()
+            scan()
+        else:
+            sdm.sdm_forward(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M, y,
+                            idx_w, wt_w, idx_r, wt_r, workspace=wsp, stream=stream)
 
     def barrier():
         if ws > 1:
@@ -298,11 +334,17 @@ def run_ours(args, w):
             return sum(a.elapsed_time(b) for a, b in evs) / n
 
         nk = max(3, min(args.steps, 20))
-        t_addr = per_call(lambda: sdm.sdm_address(sh, g["q_w"], g["q_r"], g["K"], idx_w, wt_w,
-                                                  idx_r, wt_r, stream=stream), nk)
-        t_scan = per_call(lambda: sdm.sdm_scan(sh, idx_w, wt_w, idx_r, wt_r, g["alpha"],
-                                               g["beta"], g["v"], M, y, workspace=wsp,
-                                               stream=stream), nk)
+        kernels = {}
+        if args.variant == "decode":
+            t_main = per_call(forward, nk)
+            kernels["sdm_decode"] = t_main
+        else:
+            kernels["sdm_address"] = per_call(address, nk)
+            t_main = per_call(scan, nk)
+            kernels["sdm_scan_logged" if undo is not None else "sdm_scan"] = t_main
+            if undo is not None:
+                kernels["sdm_scan_undo"] = per_call(
+                    lambda: sdm.sdm_scan_undo(sh, idx_w, undo, M, workspace=uws, stream=stream), nk)
 
         # ---- end to end through the public API with host buffers.
         host = {k: g[k].cpu().pin_memory() for k in ("q_w", "q_r", "alpha", "beta", "v")}
@@ -334,23 +376,32 @@ def run_ours(args, w):
     value = job_tokens_per_s(tokens, ws, args.steps, ms)
     peak, peak_kind = measured_peaks()
     bytes_launch = scan_bytes_per_token_head(w) * w.B * w.H * w.T
-    achieved = bytes_launch / (t_scan / 1e3) / 1e9
-    traffic = traffic_for(os.path.join(ROOT, "sparse_state_linear_gb300", "csrc", "scan.cu"))
+    if undo is not None:
+        bytes_launch += w.B * w.H * w.T * w.W * w.d_v * 4      # the log rows
+    achieved = bytes_launch / (t_main / 1e3) / 1e9
+    kname = {"decode": "sdm_decode (fused addressing + write + read)",
+             "logged": "sdm_scan_logged (plan + scan kernels, undo log)"}.get(
+                 args.variant, "sdm_scan (plan + scan kernels)")
+    traffic = None
+    if args.variant in ("forward", "fig2") and w.name == "gdn_matched" and w.update_form == 0:
+        traffic = traffic_for(os.path.join(ROOT, "sparse_state_linear_gb300", "csrc", "scan.cu"))
+    launches = {"decode": 1, "logged": 3}.get(args.variant, 3)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; bf16 inputs, fp32 table)" if w.bf16 else "synthetic (seeded, fp32)",
-        "config": dict(config_of(w), parallelism=f"dp{ws}" if ws > 1 else "single"),
+        "config": dict(config_of(w), variant=args.variant,
+                       parallelism=f"dp{ws}" if ws > 1 else "single"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "sdm_scan (plan + scan kernels)",
+                     "kernel": kname,
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": bytes_launch},
-        "kernels_ms": {"sdm_address": t_addr, "sdm_scan": t_scan},
+        "kernels_ms": kernels,
         "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
     }
     if ws == 1 and rank == 0 and not args.no_cpu_baseline:
@@ -371,13 +422,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gdn_matched", choices=sorted(WORKLOADS))
+    ap.add_argument("--variant", default="forward", choices=["forward", "fig2", "logged", "decode"],
+                    help="forward: sdm_forward (the headline); fig2: the same with the Fig. 2 "
+                         "update form; logged: addressing + scan with the undo log (undo timed "
+                         "apart); decode: sdm_decode on a one-token-per-sequence workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    w = WORKLOADS[args.workload]
+    w = variant_workload(args)
     if args.impl == "reference":
         run_reference(args, w)
     else:

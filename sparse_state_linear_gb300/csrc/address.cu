@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
           if (item >= BT) continue;
           const int k = sg == 0 ? d.kw : d.kr;
           RowSrc src{sc + (size_t)rr * scs};
-          warp_topk<16>(src, d.s, k, ws, lane);
+          warp_topk<8>(src, d.s, k, ws, lane);   // s <= 256 here
           float* ov = lv + (rr * 2 + p) * kMaxSel;
           uint32_t* oi = lid + (rr * 2 + p) * kMaxSel;
           for (int e = lane; e < k; e += 32) {

@@ -346,29 +346,75 @@ def run_ours(args, w):
                 kernels["sdm_scan_undo"] = per_call(
                     lambda: sdm.sdm_scan_undo(sh, idx_w, undo, M, workspace=uws, stream=stream), nk)
 
-        # ---- end to end through the public API with host buffers.
-        host = {k: g[k].cpu().pin_memory() for k in ("q_w", "q_r", "alpha", "beta", "v")}
-        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        # ---- end to end through the public API with host buffers: every
+        # step copies its inputs from pinned host memory and its y back.  The
+        # copies run on a second stream, double-buffered, so step i's compute
+        # overlaps step i+1's upload and step i-1's download (the table is
+        # carried in place, in order, on the compute stream).
+        names = ("q_w", "q_r", "alpha", "beta", "v")
+        host = {k: g[k].cpu().pin_memory() for k in names}
+        bufs = [{k: torch.empty_like(g[k]) for k in names} for _ in range(2)]
+        y_dev = [torch.empty_like(y) for _ in range(2)]
+        y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = y_host.numel() * y_host.element_size()
-        ne = max(3, min(args.steps, 20))
+        d2h = y_host[0].numel() * y_host[0].element_size()
+        ne = max(4, min(args.steps, 20))
+        copy = torch.cuda.Stream(dev)
+        g_keep = dict(g)
 
-        def e2e_step():
-            for k, t in host.items():
-                g[k].copy_(t, non_blocking=True)
-            forward()
-            y_host.copy_(y, non_blocking=True)
+        def run_e2e(n):
+            up = [torch.cuda.Event() for _ in range(n)]
+            done = [torch.cuda.Event() for _ in range(n)]
+            down = [torch.cuda.Event() for _ in range(n)]
+            for i in range(n + 1):
+                if i < n:
+                    with torch.cuda.stream(copy):
+                        if i >= 2:
+                            copy.wait_event(done[i - 2])     # buffer i%2 is free again
+                        for k in names:
+                            bufs[i % 2][k].copy_(host[k], non_blocking=True)
+                        up[i].record(copy)
+                if i >= 1:
+                    j = i - 1
+                    with torch.cuda.stream(copy):
+                        copy.wait_event(done[j])
+                        y_host[j % 2].copy_(y_dev[j % 2], non_blocking=True)
+                        down[j].record(copy)
+                if i < n:
+                    stream.wait_event(up[i])
+                    if i >= 2:
+                        stream.wait_event(down[i - 2])     # y buffer i%2 was read back
+                    for k in names:
+                        g[k] = bufs[i % 2][k]
+                    forward_to(y_dev[i % 2])
+                    done[i].record(stream)
+            return down[n - 1]
 
-        e2e_step()
+        def forward_to(ydst):
+            if args.variant == "decode":
+                sdm.sdm_decode(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M,
+                               ydst, idx_w, wt_w, idx_r, wt_r, stream=stream)
+            elif undo is not None:
+                sdm.sdm_address(sh, g["q_w"], g["q_r"], g["K"], idx_w, wt_w, idx_r, wt_r,
+                                stream=stream)
+                sdm.sdm_scan_logged(sh, idx_w, wt_w, idx_r, wt_r, g["alpha"], g["beta"], g["v"],
+                                    M, ydst, undo=undo, workspace=wsp, stream=stream)
+            else:
+                sdm.sdm_forward(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"],
+                                M, ydst, idx_w, wt_w, idx_r, wt_r, workspace=wsp, stream=stream)
+
+        run_e2e(2)
         torch.cuda.synchronize(dev)
         barrier()
         a, b = ev(), ev()
         a.record(stream)
-        for _ in range(ne):
-            e2e_step()
+        copy.wait_event(a)                     # no upload starts before the timed region
+        last = run_e2e(ne)
+        stream.wait_event(last)
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = a.elapsed_time(b) / ne
+        g.update(g_keep)
     if status != 0:
         raise RuntimeError(f"device reported status {status} in the timed region")
 

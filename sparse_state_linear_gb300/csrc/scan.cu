@@ -30,10 +30,12 @@
 //    slot repeated within one write set).  One CTA hashes the write sets of
 //    a block of steps plus the depth-1 steps before it into shared memory
 //    and answers every lookup of the block in parallel.
-//  * scan_kernel, one CTA per unit: 8 consumer warps and 1 producer warp.
-//    The producer copies each step's slot lists, weights, codes and value
-//    slice into a ring of metadata slots (cp.async, several steps ahead) and
-//    turns codes into shared-memory offsets.  The consumers fetch the rows of
+//  * scan_kernel, one CTA per unit: 8 consumer warps, 1 producer warp and 4
+//    loader warps.  The producer copies each step's slot lists, weights,
+//    codes and value slice into a ring of metadata slots (cp.async, several
+//    steps ahead) and adds the gates; every loader and consumer thread turns
+//    the plan codes of the rows it handles into shared-memory places itself,
+//    so the producer's per-step work stays short.  The consumers fetch the rows of
 //    step t+depth right after step t (cp.async, 16 B per lane, coalesced per
 //    row slice; each lane fetches exactly the chunks it later uses), so depth
 //    steps of row traffic are in flight per unit.  A step is: wait for own
@@ -53,9 +55,6 @@ constexpr int kLoaders = 128;    // loader threads (4 warps) that fetch the rows
 constexpr int kThreads = kConsumers + 32 + kLoaders;
 constexpr int kP = 4;            // producer's metadata prefetch distance (steps)
 constexpr int kSlack = 4;        // steps the producer may prepare beyond the need
-constexpr uint32_t kFwd = 1u << 30;   // src flag: forwarded, do not fetch
-constexpr uint32_t kSkip = 1u << 31;  // src flag: invalid row, ignore
-constexpr uint32_t kOffMask = 0x00ffffffu;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 
 // Plan kernel.
@@ -64,19 +63,18 @@ constexpr int kPlanThreads = 256;
 constexpr int kPlanHash = 16384;     // hash entries (uint32) in shared memory
 constexpr uint32_t kPlanEmpty = 0xffffffffu;
 
+// One step's metadata.  Every array starts on a 16-byte boundary (16-byte
+// cp.async destinations).
 struct MetaSlot {
   int32_t idx_w[64];
-  int32_t idx_r[64];
   float wt_w[64];
+  int32_t idx_r[64];
   float wt_r[64];
-  uint32_t src_w[64];     // shared-memory byte offset of the row's chunk 0 | flags
-  uint32_t src_r[64];
   int16_t code[128];      // plan codes: W write rows then R read rows
   unsigned char vraw[256];
   float alpha, beta, pad0, pad1;
-  unsigned char pad[112];
 };
-static_assert(sizeof(MetaSlot) == 2176, "meta slot size");
+static_assert(sizeof(MetaSlot) == 1552, "meta slot size");
 
 struct ScanArgs {
   Dims d;
@@ -270,12 +268,15 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
       ga_nxt = load_scalar(A.alpha, th0 + 32 + lane, d.in_dtype);
       gb_nxt = load_scalar(A.beta, th0 + 32 + lane, d.in_dtype);
     }
-    const bool vec_w = (W & 3) == 0, vec_r = (R & 3) == 0;
+    // Slot lists, weights, codes and the value slice of step u: 16-byte
+    // cp.async when every array is a whole number of 16-byte units, else
+    // 4-byte cp.async per element.
+    const bool vec = (W & 3) == 0 && (R & 3) == 0;
+    const uint32_t vbytes = (uint32_t)(CW * IB);
     Ring mi{0, MR, 0u};         // slot of step u (copy stage)
-    Ring mp{0, MR, 0u};         // slot of step up = u - kP (decode stage)
-    Ring wp{0, NS, 0u};         // write-tile slot of step up
-    Ring rp{0, D, 0u};          // read-tile slot of step up
-    for (int u = 0; u < T + kP; ++u) {
+    Ring mp{0, MR, 0u};         // slot of step up = u - kP (publish stage)
+    bool failed = false;
+    for (int u = 0; u < T + kP && !failed; ++u) {
       if (u < T) {
         if (u >= MR) {
           // Slot reuse: step u - MR must be finished by the consumers.
@@ -289,47 +290,45 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
           }
           if (!ok) {
             record_status(A.status, SDM_ERR_TIMEOUT);
+            failed = true;
             break;
           }
         }
         MetaSlot* m = meta + mi.i;
         const size_t th = th0 + u;
-        if (vec_w) {
+        const unsigned char* vsrc =
+            reinterpret_cast<const unsigned char*>(A.v) + (th * dv + c0) * IB;
+        if (vec) {
           for (int c = lane; c < W / 4; c += 32) {
             cp_async16(&m->idx_w[4 * c], A.idx_w + th * W + 4 * c);
             cp_async16(&m->wt_w[4 * c], A.wt_w + th * W + 4 * c);
+          }
+          for (int c = lane; c < R / 4; c += 32) {
+            cp_async16(&m->idx_r[4 * c], A.idx_r + th * R + 4 * c);
+            cp_async16(&m->wt_r[4 * c], A.wt_r + th * R + 4 * c);
           }
         } else {
           for (int j = lane; j < W; j += 32) {
             cp_async4(&m->idx_w[j], A.idx_w + th * W + j);
             cp_async4(&m->wt_w[j], A.wt_w + th * W + j);
           }
-        }
-        if (vec_r) {
-          for (int c = lane; c < R / 4; c += 32) {
-            cp_async16(&m->idx_r[4 * c], A.idx_r + th * R + 4 * c);
-            cp_async16(&m->wt_r[4 * c], A.wt_r + th * R + 4 * c);
-          }
-        } else {
           for (int j = lane; j < R; j += 32) {
             cp_async4(&m->idx_r[j], A.idx_r + th * R + j);
             cp_async4(&m->wt_r[j], A.wt_r + th * R + j);
           }
         }
         if (lane < CP / 8) cp_async16(&m->code[8 * lane], A.codes + th * CP + 8 * lane);
-        if (lane < CW * IB / 16)
-          cp_async16(m->vraw + 16 * lane,
-                     reinterpret_cast<const unsigned char*>(A.v) + (th * dv + c0) * IB + 16 * lane);
+        if (lane < (int)vbytes / 16) cp_async16(m->vraw + 16 * lane, vsrc + 16 * lane);
         mi.next();
       }
       cp_async_commit();
       if (u < kP) continue;
 
-      // ---- step up: gates, and the shared-memory source of every row.
+      // ---- step up: its metadata has landed; add the gates and publish.
       const int up = u - kP;
+      MetaSlot* m = meta + mp.i;
       cp_async_wait<kP>();
       __syncwarp();
-      MetaSlot* m = meta + mp.i;
       if ((up & 31) == 0 && up > 0) {
         ga_cur = ga_nxt;
         gb_cur = gb_nxt;
@@ -344,29 +343,9 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
         m->alpha = ga;
         m->beta = gb;
       }
-      const int wcur = wp.i;
-      const uint32_t wbase = (uint32_t)L.wtile, rbase = (uint32_t)L.rtile + rp.i * rslot;
-      for (int k = lane; k < W + R; k += 32) {
-        const int c = m->code[k];
-        uint32_t src;
-        if (c == -2) {
-          src = kSkip;
-        } else if (c >= 0) {
-          const int dd = c >> 6, p = c & 63;
-          const int sl = wcur >= dd ? wcur - dd : wcur - dd + NS;
-          src = (wbase + sl * wslot + p * rowb) | kFwd;
-        } else if (k < W) {
-          src = wbase + wcur * wslot + k * rowb;
-        } else {
-          src = rbase + (k - W) * rowb;
-        }
-        if (k < W) m->src_w[k] = src; else m->src_r[k - W] = src;
-      }
       __syncwarp();
       mbar_arrive(&mfull[mp.i]);
       mp.next();
-      wp.next();
-      rp.next();
     }
     cp_async_wait_all();
     return;
@@ -380,9 +359,10 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
     const int lt = tid - (kConsumers + 32);
     const int lc = lt % CH, lr = lt / CH;
     constexpr int LRP = kLoaders / CH;       // rows per loader pass
+    constexpr int kLoadRows = (128 + LRP - 1) / LRP;   // W + R <= 128 rows a step
     float* Ml = Mc + 4 * lc;
     unsigned char* sm_l = smem + 16 * lc;
-    Ring mu{0, MR, 0u}, me{0, MR, 0u}, rf{0, D, 0u};
+    Ring mu{0, MR, 0u}, me{0, MR, 0u}, rf{0, D, 0u}, lw{0, NS, 0u};
     bool ok = true;
     for (int u = 0; u < T && ok; ++u) {
       if (lane == 0) {
@@ -396,15 +376,35 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
         break;
       }
       const MetaSlot* m = meta + mu.i;
-      for (int k = lr; k < W + R; k += LRP) {
-        const uint32_t sv = k < W ? m->src_w[k] : m->src_r[k - W];
-        const int row = k < W ? m->idx_w[k] : m->idx_r[k - W];
-        if (!(sv & (kFwd | kSkip))) cp_async16(sm_l + (sv & kOffMask), Ml + (size_t)row * dv);
+      // Only rows whose current value is in HBM (code -1) are fetched; a
+      // forwarded (>= 0) or invalid (-2) row is not.
+      // All of this thread's codes and slots are read before the first copy
+      // is issued (a copy orders later shared-memory reads behind it).
+      const uint32_t wb = (uint32_t)L.wtile + lw.i * wslot;
+      const uint32_t rb = (uint32_t)L.rtile + rf.i * rslot;
+      int code[kLoadRows], row[kLoadRows];
+#pragma unroll
+      for (int i = 0; i < kLoadRows; ++i) {
+        const int k = lr + i * LRP;
+        code[i] = -2;
+        row[i] = 0;
+        if (k < W + R) {
+          code[i] = m->code[k];
+          row[i] = k < W ? m->idx_w[k] : m->idx_r[k - W];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kLoadRows; ++i) {
+        const int k = lr + i * LRP;
+        if (code[i] != -1) continue;
+        const uint32_t off = k < W ? wb + k * rowb : rb + (k - W) * rowb;
+        cp_async16(sm_l + off, Ml + (size_t)row[i] * dv);
       }
       cp_async_mbar_arrive_noinc(&rfull[rf.i]);
       mu.next();
       if (u >= D) me.next();
       rf.next();
+      lw.next();
     }
     cp_async_wait_all();
     return;
@@ -416,6 +416,14 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
   float* Mt = Mc + 4 * myc;                  // this lane's column chunk of row 0
   unsigned char* sm_c = smem + 16 * myc;     // shared base shifted to the chunk
   bool aborted = false;
+
+  // Shared-memory place of a forwarded row: position p of the write tile of
+  // step t - dd, for plan code (dd << 6) | p; wcur is step t's write tile.
+  auto fwd_place = [&](int code, int wcur) -> const unsigned char* {
+    const int dd = code >> 6, p = code & 63;
+    const int sl = wcur >= dd ? wcur - dd : wcur - dd + NS;
+    return sm_c + L.wtile + sl * wslot + p * rowb;
+  };
 
   auto finalize = [&](int t) {
     if (lane < CH) {
@@ -459,14 +467,12 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
       for (int pw = 0; pw < PW; ++pw) {
         const int j = pw * RP + myr;
         if (j >= W) break;
-        const uint32_t s = m->src_w[j];
+        const int code = m->code[j];
         const int row = m->idx_w[j];
         const float wj = m->wt_w[j];
         float4 x = *reinterpret_cast<const float4*>(wdst + j * rowb);   // fetched copy
-        if (s & (kFwd | kSkip)) {
-          if (s & kSkip) continue;
-          x = *reinterpret_cast<const float4*>(sm_c + (s & kOffMask));  // forwarded copy
-        }
+        if (code == -2) continue;                                       // invalid row
+        if (code >= 0) x = *reinterpret_cast<const float4*>(fwd_place(code, wt.i));  // forwarded
         if (A.undo)
           *reinterpret_cast<float4*>(A.undo + ((th0 + t) * W + j) * dv + c0 + 4 * myc) = x;
         const float cw = b * wj;
@@ -494,10 +500,10 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
           const int j = pw * RP + myr;
           md[pw] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (j >= W) continue;
-          const uint32_t s = m->src_w[j];
-          if (s & kSkip) continue;
-          const float4 x = *reinterpret_cast<const float4*>(
-              (s & kFwd) ? sm_c + (s & kOffMask) : wdst + j * rowb);
+          const int code = m->code[j];
+          float4 x = *reinterpret_cast<const float4*>(wdst + j * rowb);
+          if (code == -2) continue;
+          if (code >= 0) x = *reinterpret_cast<const float4*>(fwd_place(code, wt.i));
           if (A.undo)
             *reinterpret_cast<float4*>(A.undo + ((th0 + t) * W + j) * dv + c0 + 4 * myc) = x;
           const float wj = m->wt_w[j];
@@ -538,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
       for (int pw = 0; pw < kMaxPW; ++pw) {
         const int j = pw * RP + myr;
         if (j >= W) continue;
-        if (m->src_w[j] & kSkip) continue;
+        if (m->code[j] == -2) continue;
         const int row = m->idx_w[j];
         const float cw = b * m->wt_w[j];
         float4 o;
@@ -563,10 +569,11 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
     for (int pr = 0; pr < PR; ++pr) {
       const int q = pr * RP + myr;
       if (q >= R) break;
-      const uint32_t s = m->src_r[q];
+      const int code = m->code[W + q];
       const float w = m->wt_r[q];
-      if (s & kSkip) continue;
-      const float4 x = *reinterpret_cast<const float4*>(sm_c + (s & kOffMask));
+      float4 x = *reinterpret_cast<const float4*>(sm_c + L.rtile + rf.i * rslot + q * rowb);
+      if (code == -2) continue;
+      if (code >= 0) x = *reinterpret_cast<const float4*>(fwd_place(code, wt.i));
       acc.x = fmaf(w, x.x, acc.x);
       acc.y = fmaf(w, x.y, acc.y);
       acc.z = fmaf(w, x.z, acc.z);

@@ -412,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
 
   // -------------------------------------------------------------- consumers
   const int myc = tid % CH, myr = tid / CH;
-  const int PW = (W + RP - 1) / RP, PR = (R + RP - 1) / RP;
+  constexpr int kMaxPW = (64 + RP - 1) / RP;   // write / read rows per thread (W, R <= 64)
+  constexpr int kMaxPR = kMaxPW;
   float* Mt = Mc + 4 * myc;                  // this lane's column chunk of row 0
   unsigned char* sm_c = smem + 16 * myc;     // shared base shifted to the chunk
   bool aborted = false;
@@ -460,36 +461,46 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
     }
     const MetaSlot* m = meta + mt.i;
     if (!FIG2 && !aborted) {
-      // Write: decay + per-slot delta (Eq. (3)-(4)).
+      // Write: decay + per-slot delta (Eq. (3)-(4)).  Every row this thread
+      // writes is read first, so the rows' shared-memory latencies overlap.
       const float a = m->alpha, b = m->beta;
       const float4 vv = load_v4<BF16>(m->vraw, myc);
       unsigned char* wdst = sm_c + L.wtile + wt.i * wslot;
-      for (int pw = 0; pw < PW; ++pw) {
+      int code[kMaxPW], row[kMaxPW];
+      float wj[kMaxPW];
+      float4 x[kMaxPW];
+#pragma unroll
+      for (int pw = 0; pw < kMaxPW; ++pw) {
         const int j = pw * RP + myr;
-        if (j >= W) break;
-        const int code = m->code[j];
-        const int row = m->idx_w[j];
-        const float wj = m->wt_w[j];
-        float4 x = *reinterpret_cast<const float4*>(wdst + j * rowb);   // fetched copy
-        if (code == -2) continue;                                       // invalid row
-        if (code >= 0) x = *reinterpret_cast<const float4*>(fwd_place(code, wt.i));  // forwarded
+        code[pw] = -2;
+        if (j < W) {
+          code[pw] = m->code[j];
+          row[pw] = m->idx_w[j];
+          wj[pw] = m->wt_w[j];
+          x[pw] = *reinterpret_cast<const float4*>(wdst + j * rowb);   // fetched copy
+        }
+      }
+#pragma unroll
+      for (int pw = 0; pw < kMaxPW; ++pw) {
+        const int j = pw * RP + myr;
+        if (code[pw] == -2) continue;                                   // absent / invalid
+        if (code[pw] >= 0) x[pw] = *reinterpret_cast<const float4*>(fwd_place(code[pw], wt.i));
         if (A.undo)
-          *reinterpret_cast<float4*>(A.undo + ((th0 + t) * W + j) * dv + c0 + 4 * myc) = x;
-        const float cw = b * wj;
+          *reinterpret_cast<float4*>(A.undo + ((th0 + t) * W + j) * dv + c0 + 4 * myc) = x[pw];
+        const float cw = b * wj[pw];
         float4 o;
         float mt_;
-        mt_ = a * x.x; o.x = fmaf(cw, vv.x - mt_, mt_);
-        mt_ = a * x.y; o.y = fmaf(cw, vv.y - mt_, mt_);
-        mt_ = a * x.z; o.z = fmaf(cw, vv.z - mt_, mt_);
-        mt_ = a * x.w; o.w = fmaf(cw, vv.w - mt_, mt_);
+        mt_ = a * x[pw].x; o.x = fmaf(cw, vv.x - mt_, mt_);
+        mt_ = a * x[pw].y; o.y = fmaf(cw, vv.y - mt_, mt_);
+        mt_ = a * x[pw].z; o.z = fmaf(cw, vv.z - mt_, mt_);
+        mt_ = a * x[pw].w; o.w = fmaf(cw, vv.w - mt_, mt_);
         *reinterpret_cast<float4*>(wdst + j * rowb) = o;
-        *reinterpret_cast<float4*>(Mt + (size_t)row * dv) = o;
+        *reinterpret_cast<float4*>(Mt + (size_t)row[pw] * dv) = o;
       }
     }
     if (FIG2) {
       // Write, Fig. 2 form: decay every write row, reduce the shared
       // prediction vhat over the write set, then one residual for all rows.
-      constexpr int kMaxPW = (64 + RP - 1) / RP;
       float4 md[kMaxPW];
       const float a = m->alpha;
       unsigned char* wdst = sm_c + L.wtile + wt.i * wslot;
@@ -564,20 +575,32 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
     }
     if (t > 0 && warp == ((t - 1) & 7)) finalize(t - 1);
 
-    // Read after the write (Eq. (5)).
+    // Read after the write (Eq. (5)); all of this thread's rows are read first.
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int pr = 0; pr < PR; ++pr) {
-      const int q = pr * RP + myr;
-      if (q >= R) break;
-      const int code = m->code[W + q];
-      const float w = m->wt_r[q];
-      float4 x = *reinterpret_cast<const float4*>(sm_c + L.rtile + rf.i * rslot + q * rowb);
-      if (code == -2) continue;
-      if (code >= 0) x = *reinterpret_cast<const float4*>(fwd_place(code, wt.i));
-      acc.x = fmaf(w, x.x, acc.x);
-      acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z);
-      acc.w = fmaf(w, x.w, acc.w);
+    {
+      int code[kMaxPR];
+      float w[kMaxPR];
+      float4 x[kMaxPR];
+      const unsigned char* rsrc = sm_c + L.rtile + rf.i * rslot;
+#pragma unroll
+      for (int pr = 0; pr < kMaxPR; ++pr) {
+        const int q = pr * RP + myr;
+        code[pr] = -2;
+        if (q < R) {
+          code[pr] = m->code[W + q];
+          w[pr] = m->wt_r[q];
+          x[pr] = *reinterpret_cast<const float4*>(rsrc + q * rowb);
+        }
+      }
+#pragma unroll
+      for (int pr = 0; pr < kMaxPR; ++pr) {
+        if (code[pr] == -2) continue;
+        if (code[pr] >= 0) x[pr] = *reinterpret_cast<const float4*>(fwd_place(code[pr], wt.i));
+        acc.x = fmaf(w[pr], x[pr].x, acc.x);
+        acc.y = fmaf(w[pr], x[pr].y, acc.y);
+        acc.z = fmaf(w[pr], x[pr].z, acc.z);
+        acc.w = fmaf(w[pr], x[pr].w, acc.w);
+      }
     }
 #pragma unroll
     for (int off = CH; off < 32; off <<= 1) {

@@ -324,7 +324,7 @@ cudaError_t launch_t(const AddrArgs& A, cudaStream_t stream) {
 // memory columns; rows are then staged 32 at a time through padded shared
 // memory for the warp selection and merge above.
 constexpr int kTcRows = 128;
-constexpr int kTcThreads = 512;
+constexpr int kTcThreads = 1024;
 
 struct TcLayout {
   size_t a, b, sc, lv, lid, ws, stair, nst, bar, tslot, total;
@@ -335,13 +335,18 @@ __host__ __device__ inline TcLayout tc_layout(int s, int dh) {
   TcLayout L;
   L.spad = (s + 15) & ~15;     // MMA N
   L.scs = L.spad + 4;          // staged row stride in floats (16-byte rows, no bank conflicts)
+  // The MMA operands are dead once the MMA has completed, before any
+  // selection starts: the warps' selection scratch overlays them.
   size_t o = 0;
   L.a = o;     o = align_up(o + (size_t)2 * kTcRows * dh * 2, 1024);
   L.b = o;     o = align_up(o + (size_t)2 * L.spad * dh * 2, 1024);
+  L.ws = 0;
+  o = align_up(o > sizeof(WarpScratch) * (kTcThreads / 32) ? o
+                                                          : sizeof(WarpScratch) * (kTcThreads / 32),
+               1024);
   L.sc = o;    o = align_up(o + sizeof(float) * 32 * (size_t)L.scs, 16);
   L.lv = o;    o = align_up(o + sizeof(float) * 32 * 2 * kMaxSel, 16);
   L.lid = o;   o = align_up(o + sizeof(uint32_t) * 32 * 2 * kMaxSel, 16);
-  L.ws = o;    o = align_up(o + sizeof(WarpScratch) * (kTcThreads / 32), 16);
   L.stair = o; o = align_up(o + sizeof(uint16_t) * 2 * kStairMax, 16);
   L.nst = o;   o = align_up(o + sizeof(int) * 2, 16);
   L.bar = o;   o = align_up(o + sizeof(uint64_t), 16);
@@ -444,8 +449,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
                      ks > 0);
     tc::commit(bar);
   }
-  if (!mbar_wait_bounded(bar, 0, 4000000000ull)) record_status(A.status, SDM_ERR_TIMEOUT);
+  if (!mbar_wait_bounded(bar, 0, 4000000000ull)) {
+    record_status(A.status, SDM_ERR_TIMEOUT);
+    mbar_wait_bounded(bar, 0, 1000000000ull);   // drain before the operands are reused
+  }
   tc::fence_after_sync();
+  tc::fence_smem_to_async();
 
   if (MODE == kAddrScoresOnly) {
     // Warps 0-3: half 0, warps 4-7: half 1; lane = row.
@@ -459,8 +468,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
       const long long b = item / d.T, t = item - b * d.T;
       th = (b * d.H + h) * d.T + t;
     }
-    // Warps 8-15 take the second half of the columns.
-    for (int c0 = 16 * (warp >> 3); c0 < spad; c0 += 32) {
+    // Warps 8w .. 8w+7 take every (kTcThreads / 256)-th block of 16 columns.
+    for (int c0 = 16 * (warp >> 3); c0 < spad; c0 += 16 * (kTcThreads / 256)) {
       float v[16];
       tc::ld16(tmem + ((uint32_t)(32 * g) << 16) + p * cstride + c0, v);
       if (item < BT)

@@ -287,7 +287,11 @@ __device__ bool warp_topk_bucketed(const Src& src, int n, int k, WarpScratch& ws
     const float dd = (vmax - x) * scale;
     return min(255u, __float2uint_rz(dd));
   };
-  for (int i = lane; i < 256; i += 32) ws.hist[i] = 0u;
+  {
+    uint4* h4 = reinterpret_cast<uint4*>(ws.hist);
+    h4[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+    h4[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+  }
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < PL; ++i)
@@ -295,11 +299,14 @@ __device__ bool warp_topk_bucketed(const Src& src, int n, int k, WarpScratch& ws
   __syncwarp();
   // Exclusive prefix over buckets (lane owns 8 consecutive buckets).
   uint32_t c[8], tot = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    c[i] = ws.hist[8 * lane + i];
-    tot += c[i];
+  {
+    const uint4 a = reinterpret_cast<const uint4*>(ws.hist)[2 * lane];
+    const uint4 b = reinterpret_cast<const uint4*>(ws.hist)[2 * lane + 1];
+    c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
+    c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
   }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tot += c[i];
   uint32_t inc = tot;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -308,13 +315,22 @@ __device__ bool warp_topk_bucketed(const Src& src, int n, int k, WarpScratch& ws
   }
   uint32_t run = inc - tot;
   uint32_t bstar = 256;          // boundary bucket (found by exactly one lane)
+  uint32_t pre[8];
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    ws.base[8 * lane + i] = run;
-    ws.hist[8 * lane + i] = run;   // from here on: scatter cursors
+    pre[i] = run;
     if (run < (uint32_t)k && (uint32_t)k <= run + c[i]) bstar = 8 * lane + i;
     run += c[i];
+  }
+  {
+    // Bucket bases; the histogram becomes the scatter cursors.
+    const uint4 a = make_uint4(pre[0], pre[1], pre[2], pre[3]);
+    const uint4 b = make_uint4(pre[4], pre[5], pre[6], pre[7]);
+    reinterpret_cast<uint4*>(ws.base)[2 * lane] = a;
+    reinterpret_cast<uint4*>(ws.base)[2 * lane + 1] = b;
+    reinterpret_cast<uint4*>(ws.hist)[2 * lane] = a;
+    reinterpret_cast<uint4*>(ws.hist)[2 * lane + 1] = b;
   }
   if (lane == 31) ws.base[256] = run;
 #pragma unroll

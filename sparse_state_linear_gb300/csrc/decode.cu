@@ -31,10 +31,10 @@
 namespace sdm {
 namespace {
 
-constexpr int kDecThreads = 256;
+constexpr int kDecThreads = 512;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kStairCap = 320;   // >= sum_{a<64} floor(64/(a+1)) = 280
-constexpr int kBatch = 16;       // table rows in flight per thread
+constexpr int kBatch = 8;        // table rows in flight per thread
 
 struct DecArgs {
   Dims d;
@@ -58,7 +58,7 @@ struct DecArgs {
 };
 
 struct DecLayout {
-  size_t q, S, lv, lid, ws, stair, nst, sel, red, total;
+  size_t q, S, lv, lid, ws, stair, nst, sel, red, part, total;
 };
 
 __host__ __device__ inline size_t dl_align(size_t x) { return (x + 15) / 16 * 16; }
@@ -75,6 +75,7 @@ __host__ __device__ inline DecLayout dec_layout(int s, int dh) {
   L.nst = o;   o = dl_align(o + sizeof(int) * 2);
   L.sel = o;   o = dl_align(o + sizeof(float) * 4 * kMaxSel);   // idx_w, wt_w, idx_r, wt_r
   L.red = o;   o = dl_align(o + sizeof(float) * kDecWarps);
+  L.part = o;  o = dl_align(o + sizeof(float) * 4 * kDecThreads);   // row-group partials
   L.total = o;
   return L;
 }
@@ -152,12 +153,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
   int32_t* sidx = reinterpret_cast<int32_t*>(smem + L.sel);      // [2][64]
   float* swt = reinterpret_cast<float*>(smem + L.sel) + 2 * kMaxSel;
   float* red = reinterpret_cast<float*>(smem + L.red);
+  float4* part = reinterpret_cast<float4*>(smem + L.part);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chain = blockIdx.x;              // b * H + h
   const int h = chain % d.H;
   const int s = d.s, dh = d.dh, dv = d.dv, W = d.W, R = d.R;
   const int nc4 = dv / 4;
+  // Write / read work items: (column chunk c4, row group rg); the G row
+  // groups of a chunk split its rows and combine partial sums on chip.
+  const int G = kDecThreads / nc4;           // >= 1 (d_v <= 2048)
+  const int c4 = tid % nc4, rg = tid / nc4;
+  const bool worker = rg < G;
   float* Mc = A.M + (size_t)chain * (size_t)d.N() * dv;
   const bool fig2 = d.update == SDM_UPDATE_SHARED_RESIDUAL;
 
@@ -245,41 +252,61 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
     }
     __syncthreads();
 
-    // ---- write (Eq. (3)-(4), or the Fig. 2 form)
+    // ---- write (Eq. (3)-(4), or the Fig. 2 form): group rg takes rows
+    // j = rg, rg + G, ...; the Fig. 2 prediction is summed over the groups.
     const float a = load_scalar(A.alpha, th, d.in_dtype);
     const float bt = load_scalar(A.beta, th, d.in_dtype);
-    for (int c4 = tid; c4 < nc4; c4 += kDecThreads) {
-      const float4 vv = ld_in4<BF16>(A.v, th * nc4 + c4);
-      float4 res = vv;
-      if (fig2) {
-        float4 vh = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j0 = 0; j0 < W; j0 += kBatch) {
+    float4 vv = make_float4(0.f, 0.f, 0.f, 0.f), res = vv;
+    if (worker) {
+      vv = ld_in4<BF16>(A.v, th * nc4 + c4);
+      res = vv;
+    }
+    if (fig2) {
+      float4 vh = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (worker) {
+        for (int j0 = rg; j0 < W; j0 += kBatch * G) {
           float4 x[kBatch];
 #pragma unroll
           for (int u = 0; u < kBatch; ++u)
-            if (j0 + u < W)
-              x[u] = reinterpret_cast<const float4*>(Mc + (size_t)sidx[j0 + u] * dv)[c4];
+            if (j0 + u * G < W)
+              x[u] = reinterpret_cast<const float4*>(Mc + (size_t)sidx[j0 + u * G] * dv)[c4];
 #pragma unroll
           for (int u = 0; u < kBatch; ++u)
-            if (j0 + u < W) {
-              const float wj = swt[j0 + u];
+            if (j0 + u * G < W) {
+              const float wj = swt[j0 + u * G];
               vh.x = fmaf(wj, a * x[u].x, vh.x);
               vh.y = fmaf(wj, a * x[u].y, vh.y);
               vh.z = fmaf(wj, a * x[u].z, vh.z);
               vh.w = fmaf(wj, a * x[u].w, vh.w);
             }
         }
+        part[rg * nc4 + c4] = vh;
+      }
+      __syncthreads();
+      if (worker) {
+        vh = part[c4];
+        for (int g2 = 1; g2 < G; ++g2) {
+          const float4 p2 = part[g2 * nc4 + c4];
+          vh.x += p2.x;
+          vh.y += p2.y;
+          vh.z += p2.z;
+          vh.w += p2.w;
+        }
         res = make_float4(vv.x - vh.x, vv.y - vh.y, vv.z - vh.z, vv.w - vh.w);
       }
-      for (int j0 = 0; j0 < W; j0 += kBatch) {
+      __syncthreads();
+    }
+    if (worker) {
+      for (int j0 = rg; j0 < W; j0 += kBatch * G) {
         float4 x[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
-          if (j0 + u < W) x[u] = reinterpret_cast<const float4*>(Mc + (size_t)sidx[j0 + u] * dv)[c4];
+          if (j0 + u * G < W)
+            x[u] = reinterpret_cast<const float4*>(Mc + (size_t)sidx[j0 + u * G] * dv)[c4];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
-          if (j0 + u < W) {
-            const float cw = bt * swt[j0 + u];
+          if (j0 + u * G < W) {
+            const float cw = bt * swt[j0 + u * G];
             float4 o;
             float m;
             if (fig2) {
@@ -293,44 +320,52 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
               m = a * x[u].z; o.z = fmaf(cw, vv.z - m, m);
               m = a * x[u].w; o.w = fmaf(cw, vv.w - m, m);
             }
-            reinterpret_cast<float4*>(Mc + (size_t)sidx[j0 + u] * dv)[c4] = o;
+            reinterpret_cast<float4*>(Mc + (size_t)sidx[j0 + u * G] * dv)[c4] = o;
           }
       }
     }
     __syncthreads();
 
-    // ---- read after the write (Eq. (5)), then the optional epilogue
-    constexpr int kMaxC = 2;                 // d_v <= 2048: at most 2 chunks per thread
-    float4 yv[kMaxC];
-    float ss = 0.f;
-#pragma unroll
-    for (int ci = 0; ci < kMaxC; ++ci) {
-      const int c4 = tid + ci * kDecThreads;
-      yv[ci] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (c4 >= nc4) continue;
+    // ---- read after the write (Eq. (5)): group partials, summed by group 0;
+    // then the optional epilogue on the whole row.
+    if (worker) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q0 = 0; q0 < R; q0 += kBatch) {
+      for (int q0 = rg; q0 < R; q0 += kBatch * G) {
         float4 x[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
-          if (q0 + u < R)
-            x[u] = reinterpret_cast<const float4*>(Mc + (size_t)sidx[kMaxSel + q0 + u] * dv)[c4];
+          if (q0 + u * G < R)
+            x[u] = reinterpret_cast<const float4*>(
+                Mc + (size_t)sidx[kMaxSel + q0 + u * G] * dv)[c4];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
-          if (q0 + u < R) {
-            const float w = swt[kMaxSel + q0 + u];
+          if (q0 + u * G < R) {
+            const float w = swt[kMaxSel + q0 + u * G];
             acc.x = fmaf(w, x[u].x, acc.x);
             acc.y = fmaf(w, x[u].y, acc.y);
             acc.z = fmaf(w, x[u].z, acc.z);
             acc.w = fmaf(w, x[u].w, acc.w);
           }
       }
-      reinterpret_cast<float4*>(A.y + th * dv)[c4] = acc;
-      yv[ci] = acc;
-      ss = fmaf(acc.x, acc.x, ss);
-      ss = fmaf(acc.y, acc.y, ss);
-      ss = fmaf(acc.z, acc.z, ss);
-      ss = fmaf(acc.w, acc.w, ss);
+      part[rg * nc4 + c4] = acc;
+    }
+    __syncthreads();
+    float4 yv = make_float4(0.f, 0.f, 0.f, 0.f);
+    float ss = 0.f;
+    if (rg == 0) {
+      yv = part[c4];
+      for (int g2 = 1; g2 < G; ++g2) {
+        const float4 p2 = part[g2 * nc4 + c4];
+        yv.x += p2.x;
+        yv.y += p2.y;
+        yv.z += p2.z;
+        yv.w += p2.w;
+      }
+      reinterpret_cast<float4*>(A.y + th * dv)[c4] = yv;
+      ss = fmaf(yv.x, yv.x, ss);
+      ss = fmaf(yv.y, yv.y, ss);
+      ss = fmaf(yv.z, yv.z, ss);
+      ss = fmaf(yv.w, yv.w, ss);
     }
     if (A.out) {
 #pragma unroll
@@ -341,17 +376,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) tot += red[w];
       const float inv = 1.f / sqrtf(tot / (float)dv + A.eps);
-#pragma unroll
-      for (int ci = 0; ci < kMaxC; ++ci) {
-        const int c4 = tid + ci * kDecThreads;
-        if (c4 >= nc4) continue;
+      if (rg == 0) {
         const float4 gt = ld_in4<BF16>(A.g, th * nc4 + c4);
         const float4 sc = A.gamma ? __ldg(reinterpret_cast<const float4*>(A.gamma) +
                                           (size_t)h * nc4 + c4)
                                   : make_float4(1.f, 1.f, 1.f, 1.f);
         st_out4(A.out, th * nc4 + c4, A.out_dtype,
-                make_float4(yv[ci].x * inv * sc.x * gt.x, yv[ci].y * inv * sc.y * gt.y,
-                            yv[ci].z * inv * sc.z * gt.z, yv[ci].w * inv * sc.w * gt.w));
+                make_float4(yv.x * inv * sc.x * gt.x, yv.y * inv * sc.y * gt.y,
+                            yv.z * inv * sc.z * gt.z, yv.w * inv * sc.w * gt.w));
       }
     }
     __syncthreads();

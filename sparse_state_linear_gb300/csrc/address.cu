@@ -344,7 +344,7 @@ __host__ __device__ inline TcLayout tc_layout(int s, int dh) {
   o = align_up(o > sizeof(WarpScratch) * (kTcThreads / 32) ? o
                                                           : sizeof(WarpScratch) * (kTcThreads / 32),
                1024);
-  L.sc = o;    o = align_up(o + sizeof(float) * 32 * (size_t)L.scs, 16);
+  L.sc = o;    o = align_up(o + sizeof(float) * 2 * 32 * (size_t)L.scs, 16);   // both halves
   L.lv = o;    o = align_up(o + sizeof(float) * 32 * 2 * kMaxSel, 16);
   L.lid = o;   o = align_up(o + sizeof(uint32_t) * 32 * 2 * kMaxSel, 16);
   L.stair = o; o = align_up(o + sizeof(uint16_t) * 2 * kStairMax, 16);
@@ -477,39 +477,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
           if (c0 + i < d.s) A.S[(size_t)(th * 2 + p) * d.s + c0 + i] = v[i];
     }
   } else {
+    // Per group of 32 rows: the warps that own the group's tensor-memory lanes
+    // stage both halves' scores, then every warp runs one row end to end (both
+    // half top-k, merge, softmax) with no block barrier in between.
+    const int nblk = spad / 16;
     for (int g = 0; g < 4; ++g) {
-      for (int p = 0; p < 2; ++p) {
-        // Stage rows 32g .. 32g+31 of half p (warps g and g+4 share the columns).
-        if ((warp & 3) == g) {
-          for (int blk = warp >> 2; blk < spad / 16; blk += kTcThreads / 128) {
-            float v[16];
-            tc::ld16(tmem + ((uint32_t)(32 * g) << 16) + p * cstride + 16 * blk, v);
-            float4* dst = reinterpret_cast<float4*>(sc + (size_t)lane * scs + 16 * blk);
-            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-            dst[2] = make_float4(v[8], v[9], v[10], v[11]);
-            dst[3] = make_float4(v[12], v[13], v[14], v[15]);
-          }
+      if ((warp & 3) == g) {
+        for (int e = warp >> 2; e < 2 * nblk; e += kTcThreads / 128) {
+          const int p = e >= nblk, blk = e - p * nblk;
+          float v[16];
+          tc::ld16(tmem + ((uint32_t)(32 * g) << 16) + p * cstride + 16 * blk, v);
+          float4* dst = reinterpret_cast<float4*>(sc + (size_t)(p * 32 + lane) * scs + 16 * blk);
+          dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+          dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+          dst[2] = make_float4(v[8], v[9], v[10], v[11]);
+          dst[3] = make_float4(v[12], v[13], v[14], v[15]);
         }
-        __syncthreads();
-        for (int rr = warp; rr < 32; rr += kTcThreads / 32) {
-          int sg;
-          long long item;
-          tc_row_item<MODE>(32 * g + rr, sg, item);
-          if (item >= BT) continue;
-          const int k = sg == 0 ? d.kw : d.kr;
-          RowSrc src{sc + (size_t)rr * scs};
-          warp_topk<8>(src, d.s, k, ws, lane);   // s <= 256 here
-          float* ov = lv + (rr * 2 + p) * kMaxSel;
-          uint32_t* oi = lid + (rr * 2 + p) * kMaxSel;
-          for (int e = lane; e < k; e += 32) {
-            ov[e] = ws.out_v[e];
-            oi[e] = ws.out_id[e];
-          }
-          __syncwarp();
-        }
-        __syncthreads();
       }
+      __syncthreads();
       for (int rr = warp; rr < 32; rr += kTcThreads / 32) {
         int sg;
         long long item;
@@ -517,9 +502,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
         if (item >= BT) continue;
         const int k = sg == 0 ? d.kw : d.kr;
         const int nsel = sg == 0 ? d.W : d.R;
-        warp_merge(lv + (rr * 2 + 0) * kMaxSel, lid + (rr * 2 + 0) * kMaxSel,
-                   lv + (rr * 2 + 1) * kMaxSel, lid + (rr * 2 + 1) * kMaxSel, k, nsel,
-                   (uint32_t)d.s, stair + sg * kStairMax, nst[sg], ws, lane);
+        float* ov = lv + rr * 2 * kMaxSel;
+        uint32_t* oi = lid + rr * 2 * kMaxSel;
+#pragma unroll 1
+        for (int p = 0; p < 2; ++p) {
+          RowSrc src{sc + (size_t)(p * 32 + rr) * scs};
+          warp_topk<8>(src, d.s, k, ws, lane);   // s <= 256 here
+          for (int e = lane; e < k; e += 32) {
+            ov[p * kMaxSel + e] = ws.out_v[e];
+            oi[p * kMaxSel + e] = ws.out_id[e];
+          }
+          __syncwarp();
+        }
+        warp_merge(ov, oi, ov + kMaxSel, oi + kMaxSel, k, nsel, (uint32_t)d.s,
+                   stair + sg * kStairMax, nst[sg], ws, lane);
         const long long b = item / d.T, t = item - b * d.T;
         const long long th = (b * d.H + h) * d.T + t;
         int32_t* io = (sg == 0 ? A.idx_w : A.idx_r) + (size_t)th * nsel;
@@ -527,6 +523,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
         warp_softmax_store(ws, nsel, io, wo, lane);
         __syncwarp();
       }
+      __syncthreads();
     }
   }
   tc::fence_before_sync();

@@ -142,7 +142,54 @@ __device__ __forceinline__ uint32_t plan_hash(uint32_t row) {
 
 // Entry = (row << 13) | (step - s0) << 6 | position; rows < 2^18, step offsets
 // < 128 (kPlanTB + depth - 1), positions < 64.
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs P) {
+__device__ __forceinline__ void plan_insert(uint32_t* tab, int row, uint32_t N, int ds, int j) {
+  if (row < 0 || (uint32_t)row >= N) return;
+  const uint32_t key = ((uint32_t)row << 13) | ((uint32_t)ds << 6) | (uint32_t)j;
+  uint32_t h = plan_hash((uint32_t)row);
+  for (int i = 0; i < kPlanHash; ++i) {
+    if (atomicCAS(&tab[h], kPlanEmpty, key) == kPlanEmpty) break;
+    h = (h + 1) & (kPlanHash - 1);
+  }
+}
+
+// Code of row `row` at position k of step t (write rows k < W, then reads).
+__device__ __forceinline__ int plan_code(const uint32_t* tab, const PlanArgs& P, int s0, int row,
+                                         int t, int k) {
+  if (row < 0 || (uint32_t)row >= P.N) {
+    record_status(P.status, SDM_ERR_DEVICE_BOUNDS);
+    return -2;
+  }
+  // Latest writer s of this row with t-depth+1 <= s < t (<= t for reads).
+  const bool is_w = k < P.W;
+  const int lo = t - (P.depth - 1), hi = is_w ? t - 1 : t;
+  int best = -1, bp = 0;
+  bool dup = false;
+  uint32_t h = plan_hash((uint32_t)row);
+  for (int i = 0; i < kPlanHash; ++i) {
+    const uint32_t ent = tab[h];
+    if (ent == kPlanEmpty) break;
+    if ((ent >> 13) == (uint32_t)row) {
+      const int s = s0 + (int)((ent >> 6) & 127u), p = (int)(ent & 63u);
+      if (is_w && s == t && p != k) dup = true;
+      if (s >= lo && s <= hi && s > best) {
+        best = s;
+        bp = p;
+      }
+    }
+    h = (h + 1) & (kPlanHash - 1);
+  }
+  if (dup) {
+    record_status(P.status, SDM_ERR_DUPLICATE_SLOT);
+    return -2;
+  }
+  return best >= 0 ? ((t - best) << 6) | bp : -1;
+}
+
+// VEC (W and R multiples of 4): every thread first issues all of its index
+// loads as 16-byte vectors, so the CTA's reads are in flight together instead
+// of one dependent load per lookup.
+template <bool VEC>
+__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanArgs P) {
   extern __shared__ __align__(16) uint32_t tab[];
   const int chain = blockIdx.y;
   const int t0 = blockIdx.x * kPlanTB;
@@ -150,60 +197,73 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs P) {
   const int s0 = max(0, t0 - (P.depth - 1));
   const int W = P.W, R = P.R, WR = W + R, CP = code_pitch(W, R);
   const size_t base = (size_t)chain * P.T;
-  for (int i = threadIdx.x; i < kPlanHash / 4; i += kPlanThreads)
-    reinterpret_cast<uint4*>(tab)[i] = make_uint4(kPlanEmpty, kPlanEmpty, kPlanEmpty, kPlanEmpty);
-  __syncthreads();
-  const int nins = (t1 - s0) * W;
-  for (int e = threadIdx.x; e < nins; e += kPlanThreads) {
-    const int ds = e / W, j = e - ds * W;
-    const int row = __ldg(P.idx_w + (base + s0 + ds) * W + j);
-    if (row < 0 || (uint32_t)row >= P.N) continue;
-    const uint32_t key = ((uint32_t)row << 13) | ((uint32_t)ds << 6) | (uint32_t)j;
-    uint32_t h = plan_hash((uint32_t)row);
-    for (int i = 0; i < kPlanHash; ++i) {
-      if (atomicCAS(&tab[h], kPlanEmpty, key) == kPlanEmpty) break;
-      h = (h + 1) & (kPlanHash - 1);
-    }
-  }
-  __syncthreads();
+  const int nins = (t1 - s0) * W;          // write slots of steps s0 .. t1-1, contiguous
   const int nlook = (t1 - t0) * WR;
-  for (int e = threadIdx.x; e < nlook; e += kPlanThreads) {
-    const int dt = e / WR, k = e - dt * WR;
-    const int t = t0 + dt;
-    const bool is_w = k < W;
-    const int row = is_w ? __ldg(P.idx_w + (base + t) * W + k)
-                         : __ldg(P.idx_r + (base + t) * R + (k - W));
-    int code = -1;
-    if (row < 0 || (uint32_t)row >= P.N) {
-      record_status(P.status, SDM_ERR_DEVICE_BOUNDS);
-      code = -2;
-    } else {
-      // Latest writer s of this row with t-depth+1 <= s < t (<= t for reads).
-      const int lo = t - (P.depth - 1), hi = is_w ? t - 1 : t;
-      int best = -1, bp = 0;
-      bool dup = false;
-      uint32_t h = plan_hash((uint32_t)row);
-      for (int i = 0; i < kPlanHash; ++i) {
-        const uint32_t ent = tab[h];
-        if (ent == kPlanEmpty) break;
-        if ((ent >> 13) == (uint32_t)row) {
-          const int s = s0 + (int)((ent >> 6) & 127u), p = (int)(ent & 63u);
-          if (is_w && s == t && p != k) dup = true;
-          if (s >= lo && s <= hi && s > best) {
-            best = s;
-            bp = p;
-          }
-        }
-        h = (h + 1) & (kPlanHash - 1);
-      }
-      if (dup) {
-        record_status(P.status, SDM_ERR_DUPLICATE_SLOT);
-        code = -2;
-      } else if (best >= 0) {
-        code = ((t - best) << 6) | bp;
+  const int32_t* ins = P.idx_w + (base + s0) * W;
+  if constexpr (VEC) {
+    // Groups of 4 consecutive positions never straddle the write/read boundary.
+    constexpr int kIns = (kPlanTB + 15) * 64 / 4 / kPlanThreads + 1;
+    constexpr int kLook = kPlanTB * 128 / 4 / kPlanThreads;
+    int4 look[kLook], irow[kIns];
+#pragma unroll
+    for (int i = 0; i < kLook; ++i) {
+      const int g = 4 * (threadIdx.x + i * kPlanThreads);
+      if (g < nlook) {
+        const int dt = g / WR, k = g - dt * WR, t = t0 + dt;
+        const int32_t* src = k < W ? P.idx_w + (base + t) * W + k : P.idx_r + (base + t) * R + (k - W);
+        look[i] = __ldg(reinterpret_cast<const int4*>(src));
       }
     }
-    P.codes[(base + t) * CP + k] = (int16_t)code;
+#pragma unroll
+    for (int i = 0; i < kIns; ++i) {
+      const int g = 4 * (threadIdx.x + i * kPlanThreads);
+      if (g < nins) irow[i] = __ldg(reinterpret_cast<const int4*>(ins + g));
+    }
+    for (int i = threadIdx.x; i < kPlanHash / 4; i += kPlanThreads)
+      reinterpret_cast<uint4*>(tab)[i] = make_uint4(kPlanEmpty, kPlanEmpty, kPlanEmpty, kPlanEmpty);
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kIns; ++i) {
+      const int g = 4 * (threadIdx.x + i * kPlanThreads);
+      if (g < nins) {
+        const int ds = g / W, j = g - ds * W;
+        plan_insert(tab, irow[i].x, P.N, ds, j);
+        plan_insert(tab, irow[i].y, P.N, ds, j + 1);
+        plan_insert(tab, irow[i].z, P.N, ds, j + 2);
+        plan_insert(tab, irow[i].w, P.N, ds, j + 3);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kLook; ++i) {
+      const int g = 4 * (threadIdx.x + i * kPlanThreads);
+      if (g < nlook) {
+        const int dt = g / WR, k = g - dt * WR, t = t0 + dt;
+        const int c0 = plan_code(tab, P, s0, look[i].x, t, k);
+        const int c1 = plan_code(tab, P, s0, look[i].y, t, k + 1);
+        const int c2 = plan_code(tab, P, s0, look[i].z, t, k + 2);
+        const int c3 = plan_code(tab, P, s0, look[i].w, t, k + 3);
+        // CP is a multiple of 8 and k of 4: one aligned 8-byte store.
+        *reinterpret_cast<uint2*>(P.codes + (base + t) * CP + k) =
+            make_uint2((uint32_t)(c0 & 0xffff) | ((uint32_t)c1 << 16),
+                       (uint32_t)(c2 & 0xffff) | ((uint32_t)c3 << 16));
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < kPlanHash / 4; i += kPlanThreads)
+      reinterpret_cast<uint4*>(tab)[i] = make_uint4(kPlanEmpty, kPlanEmpty, kPlanEmpty, kPlanEmpty);
+    __syncthreads();
+    for (int e = threadIdx.x; e < nins; e += kPlanThreads) {
+      const int ds = e / W;
+      plan_insert(tab, __ldg(ins + e), P.N, ds, e - ds * W);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < nlook; e += kPlanThreads) {
+      const int dt = e / WR, k = e - dt * WR, t = t0 + dt;
+      const int row = k < W ? __ldg(P.idx_w + (base + t) * W + k)
+                            : __ldg(P.idx_r + (base + t) * R + (k - W));
+      P.codes[(base + t) * CP + k] = (int16_t)plan_code(tab, P, s0, row, t, k);
+    }
   }
 }
 
@@ -730,12 +790,14 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   int16_t* codes = static_cast<int16_t*>(workspace);
   {
     const size_t smem = sizeof(uint32_t) * kPlanHash;
-    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool vec = d.W % 4 == 0 && d.R % 4 == 0;
+    auto* kern = vec ? plan_kernel<true> : plan_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     PlanArgs P{idx_w, idx_r, codes, d.T, d.W, d.R, D, (uint32_t)d.N(), status};
     dim3 grid((unsigned)((d.T + kPlanTB - 1) / kPlanTB), (unsigned)chains);
-    plan_kernel<<<grid, kPlanThreads, smem, stream>>>(P);
+    kern<<<grid, kPlanThreads, smem, stream>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

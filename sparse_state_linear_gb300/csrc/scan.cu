@@ -59,9 +59,13 @@ constexpr uint64_t kTimeoutNs = 4000000000ull;
 
 // Plan kernel.
 constexpr int kPlanTB = 64;          // steps per plan CTA
-constexpr int kPlanThreads = 256;
+constexpr int kPlanThreads = 512;
 constexpr int kPlanHash = 16384;     // hash entries (uint32) in shared memory
 constexpr uint32_t kPlanEmpty = 0xffffffffu;
+constexpr int kPlanBloom = 2048;     // filter words (65536 bits)
+constexpr int kPlanQCap = 160;       // per-warp queue of filter hits (< 32 + 4 * 32)
+constexpr size_t kPlanSmem =
+    sizeof(uint32_t) * (kPlanHash + kPlanBloom + (kPlanThreads / 32) * kPlanQCap);
 
 // One step's metadata.  Every array starts on a 16-byte boundary (16-byte
 // cp.async destinations).
@@ -139,6 +143,8 @@ struct PlanArgs {
 __device__ __forceinline__ uint32_t plan_hash(uint32_t row) {
   return (row * 0x9E3779B1u) >> (32 - 14);
 }
+// Filter bit of a row (a different 16 bits of the same product).
+__device__ __forceinline__ uint32_t plan_bit(uint32_t row) { return (row * 0x9E3779B1u) >> 16; }
 
 // Entry = (row << 13) | (step - s0) << 6 | position; rows < 2^18, step offsets
 // < 128 (kPlanTB + depth - 1), positions < 64.
@@ -186,11 +192,16 @@ __device__ __forceinline__ int plan_code(const uint32_t* tab, const PlanArgs& P,
 }
 
 // VEC (W and R multiples of 4): every thread first issues all of its index
-// loads as 16-byte vectors, so the CTA's reads are in flight together instead
-// of one dependent load per lookup.
+// loads as 16-byte vectors, so the CTA's reads are in flight together.  Rows
+// of the block's write sets also set a bit of a 65536-bit filter; nearly
+// every lookup misses the filter (a step's rows were rarely written in the
+// few steps before it) and gets code -1 at once.  Filter hits, and rows out
+// of range, queue per warp and are resolved 32 at a time on the hash table,
+// so the probe loops run with full warps.
 template <bool VEC>
-__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanArgs P) {
+__global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P) {
   extern __shared__ __align__(16) uint32_t tab[];
+  uint32_t* bloom = tab + kPlanHash;
   const int chain = blockIdx.y;
   const int t0 = blockIdx.x * kPlanTB;
   const int t1 = min(P.T, t0 + kPlanTB);
@@ -202,8 +213,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanArgs P)
   const int32_t* ins = P.idx_w + (base + s0) * W;
   if constexpr (VEC) {
     // Groups of 4 consecutive positions never straddle the write/read boundary.
-    constexpr int kIns = (kPlanTB + 15) * 64 / 4 / kPlanThreads + 1;
+    constexpr int kIns = ((kPlanTB + 15) * 64 / 4 + kPlanThreads - 1) / kPlanThreads;
     constexpr int kLook = kPlanTB * 128 / 4 / kPlanThreads;
+    const int lane = threadIdx.x & 31;
+    uint32_t* q = bloom + kPlanBloom + (threadIdx.x >> 5) * kPlanQCap;
     int4 look[kLook], irow[kIns];
 #pragma unroll
     for (int i = 0; i < kLook; ++i) {
@@ -219,36 +232,77 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanArgs P)
       const int g = 4 * (threadIdx.x + i * kPlanThreads);
       if (g < nins) irow[i] = __ldg(reinterpret_cast<const int4*>(ins + g));
     }
-    for (int i = threadIdx.x; i < kPlanHash / 4; i += kPlanThreads)
-      reinterpret_cast<uint4*>(tab)[i] = make_uint4(kPlanEmpty, kPlanEmpty, kPlanEmpty, kPlanEmpty);
+    for (int i = threadIdx.x; i < (kPlanHash + kPlanBloom) / 4; i += kPlanThreads)
+      reinterpret_cast<uint4*>(tab)[i] = i < kPlanHash / 4 ? make_uint4(kPlanEmpty, kPlanEmpty,
+                                                                         kPlanEmpty, kPlanEmpty)
+                                                           : make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kIns; ++i) {
       const int g = 4 * (threadIdx.x + i * kPlanThreads);
       if (g < nins) {
         const int ds = g / W, j = g - ds * W;
-        plan_insert(tab, irow[i].x, P.N, ds, j);
-        plan_insert(tab, irow[i].y, P.N, ds, j + 1);
-        plan_insert(tab, irow[i].z, P.N, ds, j + 2);
-        plan_insert(tab, irow[i].w, P.N, ds, j + 3);
+        const int r4[4] = {irow[i].x, irow[i].y, irow[i].z, irow[i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (r4[e] < 0 || (uint32_t)r4[e] >= P.N) continue;
+          const uint32_t hb = plan_bit((uint32_t)r4[e]);
+          atomicOr(&bloom[hb >> 5], 1u << (hb & 31u));
+          plan_insert(tab, r4[e], P.N, ds, j + e);
+        }
       }
     }
     __syncthreads();
+    // Resolve queued hits: entry = (row << 13) | (dt * WR + k).
+    auto resolve = [&](uint32_t ent) {
+      const int row = (int)(ent >> 13), pos = (int)(ent & 8191u);
+      const int dt = pos / WR, k = pos - dt * WR, t = t0 + dt;
+      P.codes[(base + t) * CP + k] = (int16_t)plan_code(tab, P, s0, row, t, k);
+    };
+    int qn = 0;   // warp-uniform queue length
 #pragma unroll
     for (int i = 0; i < kLook; ++i) {
       const int g = 4 * (threadIdx.x + i * kPlanThreads);
+      uint32_t hit = 0;
+      int dt = 0, k = 0;
+      const int r4[4] = {look[i].x, look[i].y, look[i].z, look[i].w};
       if (g < nlook) {
-        const int dt = g / WR, k = g - dt * WR, t = t0 + dt;
-        const int c0 = plan_code(tab, P, s0, look[i].x, t, k);
-        const int c1 = plan_code(tab, P, s0, look[i].y, t, k + 1);
-        const int c2 = plan_code(tab, P, s0, look[i].z, t, k + 2);
-        const int c3 = plan_code(tab, P, s0, look[i].w, t, k + 3);
-        // CP is a multiple of 8 and k of 4: one aligned 8-byte store.
-        *reinterpret_cast<uint2*>(P.codes + (base + t) * CP + k) =
-            make_uint2((uint32_t)(c0 & 0xffff) | ((uint32_t)c1 << 16),
-                       (uint32_t)(c2 & 0xffff) | ((uint32_t)c3 << 16));
+        dt = g / WR;
+        k = g - dt * WR;
+        uint32_t c16[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          c16[e] = 0xffffu;                    // -1: the fetched copy
+          if (r4[e] < 0 || (uint32_t)r4[e] >= P.N) {
+            record_status(P.status, SDM_ERR_DEVICE_BOUNDS);
+            c16[e] = 0xfffeu;                  // -2: invalid
+          } else {
+            const uint32_t hb = plan_bit((uint32_t)r4[e]);
+            hit |= ((bloom[hb >> 5] >> (hb & 31u)) & 1u) << e;
+          }
+        }
+        // Hits are overwritten after the warp barrier below.  CP is a
+        // multiple of 8 and k of 4: one aligned 8-byte store.
+        *reinterpret_cast<uint2*>(P.codes + (base + t0 + dt) * CP + k) =
+            make_uint2(c16[0] | (c16[1] << 16), c16[2] | (c16[3] << 16));
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool h = (hit >> e) & 1u;
+        const unsigned bal = __ballot_sync(0xffffffffu, h);
+        if (h)
+          q[qn + __popc(bal & ((1u << lane) - 1u))] =
+              ((uint32_t)r4[e] << 13) | (uint32_t)(dt * WR + k + e);
+        qn += __popc(bal);
+      }
+      __syncwarp();
+      while (qn >= 32) {
+        qn -= 32;
+        resolve(q[qn + lane]);
+      }
+      __syncwarp();
     }
+    if (lane < qn) resolve(q[lane]);
   } else {
     for (int i = threadIdx.x; i < kPlanHash / 4; i += kPlanThreads)
       reinterpret_cast<uint4*>(tab)[i] = make_uint4(kPlanEmpty, kPlanEmpty, kPlanEmpty, kPlanEmpty);
@@ -789,7 +843,7 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
 
   int16_t* codes = static_cast<int16_t*>(workspace);
   {
-    const size_t smem = sizeof(uint32_t) * kPlanHash;
+    const size_t smem = kPlanSmem;
     const bool vec = d.W % 4 == 0 && d.R % 4 == 0;
     auto* kern = vec ? plan_kernel<true> : plan_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

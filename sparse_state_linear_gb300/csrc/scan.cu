@@ -60,12 +60,12 @@ constexpr uint64_t kTimeoutNs = 4000000000ull;
 // Plan kernel.
 constexpr int kPlanTB = 64;          // steps per plan CTA
 constexpr int kPlanThreads = 512;
-constexpr int kPlanHash = 16384;     // hash entries (uint32) in shared memory
-constexpr uint32_t kPlanEmpty = 0xffffffffu;
+constexpr int kPlanBuckets = 4096;   // hash buckets of 4 entries (uint32) each
 constexpr int kPlanBloom = 2048;     // filter words (65536 bits)
 constexpr int kPlanQCap = 160;       // per-warp queue of filter hits (< 32 + 4 * 32)
+// Shared memory: entries, bucket counts, filter, queues.
 constexpr size_t kPlanSmem =
-    sizeof(uint32_t) * (kPlanHash + kPlanBloom + (kPlanThreads / 32) * kPlanQCap);
+    sizeof(uint32_t) * (5 * kPlanBuckets + kPlanBloom + (kPlanThreads / 32) * kPlanQCap);
 
 // One step's metadata.  Every array starts on a 16-byte boundary (16-byte
 // cp.async destinations).
@@ -140,27 +140,34 @@ struct PlanArgs {
   unsigned* status;
 };
 
-__device__ __forceinline__ uint32_t plan_hash(uint32_t row) {
-  return (row * 0x9E3779B1u) >> (32 - 14);
+__device__ __forceinline__ uint32_t plan_bucket(uint32_t row) {
+  return (row * 0x9E3779B1u) >> 20;
 }
-// Filter bit of a row (a different 16 bits of the same product).
-__device__ __forceinline__ uint32_t plan_bit(uint32_t row) { return (row * 0x9E3779B1u) >> 16; }
+// Filter bit of a row.
+__device__ __forceinline__ uint32_t plan_bit(uint32_t row) { return (row * 0x85EBCA6Bu) >> 16; }
 
 // Entry = (row << 13) | (step - s0) << 6 | position; rows < 2^18, step offsets
-// < 128 (kPlanTB + depth - 1), positions < 64.
-__device__ __forceinline__ void plan_insert(uint32_t* tab, int row, uint32_t N, int ds, int j) {
+// < 128 (kPlanTB + depth - 1), positions < 64.  An insert claims the next
+// entry of the row's bucket by counting; a full bucket passes the entry on to
+// the next one, whose count then exceeds 4 -- which tells lookups to go on.
+__device__ __forceinline__ void plan_insert(uint32_t* tab, uint32_t* cnt, int row, uint32_t N,
+                                            int ds, int j) {
   if (row < 0 || (uint32_t)row >= N) return;
   const uint32_t key = ((uint32_t)row << 13) | ((uint32_t)ds << 6) | (uint32_t)j;
-  uint32_t h = plan_hash((uint32_t)row);
-  for (int i = 0; i < kPlanHash; ++i) {
-    if (atomicCAS(&tab[h], kPlanEmpty, key) == kPlanEmpty) break;
-    h = (h + 1) & (kPlanHash - 1);
+  uint32_t b = plan_bucket((uint32_t)row);
+  for (int i = 0; i < kPlanBuckets; ++i) {
+    const uint32_t c = atomicAdd(&cnt[b], 1u);
+    if (c < 4u) {
+      tab[4 * b + c] = key;
+      return;
+    }
+    b = (b + 1) & (kPlanBuckets - 1);
   }
 }
 
 // Code of row `row` at position k of step t (write rows k < W, then reads).
-__device__ __forceinline__ int plan_code(const uint32_t* tab, const PlanArgs& P, int s0, int row,
-                                         int t, int k) {
+__device__ __forceinline__ int plan_code(const uint32_t* tab, const uint32_t* cnt,
+                                         const PlanArgs& P, int s0, int row, int t, int k) {
   if (row < 0 || (uint32_t)row >= P.N) {
     record_status(P.status, SDM_ERR_DEVICE_BOUNDS);
     return -2;
@@ -170,19 +177,25 @@ __device__ __forceinline__ int plan_code(const uint32_t* tab, const PlanArgs& P,
   const int lo = t - (P.depth - 1), hi = is_w ? t - 1 : t;
   int best = -1, bp = 0;
   bool dup = false;
-  uint32_t h = plan_hash((uint32_t)row);
-  for (int i = 0; i < kPlanHash; ++i) {
-    const uint32_t ent = tab[h];
-    if (ent == kPlanEmpty) break;
-    if ((ent >> 13) == (uint32_t)row) {
-      const int s = s0 + (int)((ent >> 6) & 127u), p = (int)(ent & 63u);
-      if (is_w && s == t && p != k) dup = true;
-      if (s >= lo && s <= hi && s > best) {
-        best = s;
-        bp = p;
+  uint32_t b = plan_bucket((uint32_t)row);
+  for (int i = 0; i < kPlanBuckets; ++i) {
+    const uint32_t c = cnt[b];
+    const uint4 e4 = reinterpret_cast<const uint4*>(tab)[b];
+    const uint32_t ents[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t ent = ents[e];
+      if ((uint32_t)e < c && (ent >> 13) == (uint32_t)row) {
+        const int s = s0 + (int)((ent >> 6) & 127u), p = (int)(ent & 63u);
+        if (is_w && s == t && p != k) dup = true;
+        if (s >= lo && s <= hi && s > best) {
+          best = s;
+          bp = p;
+        }
       }
     }
-    h = (h + 1) & (kPlanHash - 1);
+    if (c <= 4u) break;
+    b = (b + 1) & (kPlanBuckets - 1);
   }
   if (dup) {
     record_status(P.status, SDM_ERR_DUPLICATE_SLOT);
@@ -201,7 +214,8 @@ __device__ __forceinline__ int plan_code(const uint32_t* tab, const PlanArgs& P,
 template <bool VEC>
 __global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P) {
   extern __shared__ __align__(16) uint32_t tab[];
-  uint32_t* bloom = tab + kPlanHash;
+  uint32_t* cnt = tab + 4 * kPlanBuckets;
+  uint32_t* bloom = cnt + kPlanBuckets;
   const int chain = blockIdx.y;
   const int t0 = blockIdx.x * kPlanTB;
   const int t1 = min(P.T, t0 + kPlanTB);
@@ -232,10 +246,9 @@ __global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P)
       const int g = 4 * (threadIdx.x + i * kPlanThreads);
       if (g < nins) irow[i] = __ldg(reinterpret_cast<const int4*>(ins + g));
     }
-    for (int i = threadIdx.x; i < (kPlanHash + kPlanBloom) / 4; i += kPlanThreads)
-      reinterpret_cast<uint4*>(tab)[i] = i < kPlanHash / 4 ? make_uint4(kPlanEmpty, kPlanEmpty,
-                                                                         kPlanEmpty, kPlanEmpty)
-                                                           : make_uint4(0u, 0u, 0u, 0u);
+    // Counts and filter are adjacent: one clear (entries need none).
+    for (int i = threadIdx.x; i < (kPlanBuckets + kPlanBloom) / 4; i += kPlanThreads)
+      reinterpret_cast<uint4*>(cnt)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kIns; ++i) {
@@ -248,7 +261,7 @@ __global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P)
           if (r4[e] < 0 || (uint32_t)r4[e] >= P.N) continue;
           const uint32_t hb = plan_bit((uint32_t)r4[e]);
           atomicOr(&bloom[hb >> 5], 1u << (hb & 31u));
-          plan_insert(tab, r4[e], P.N, ds, j + e);
+          plan_insert(tab, cnt, r4[e], P.N, ds, j + e);
         }
       }
     }
@@ -257,7 +270,7 @@ __global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P)
     auto resolve = [&](uint32_t ent) {
       const int row = (int)(ent >> 13), pos = (int)(ent & 8191u);
       const int dt = pos / WR, k = pos - dt * WR, t = t0 + dt;
-      P.codes[(base + t) * CP + k] = (int16_t)plan_code(tab, P, s0, row, t, k);
+      P.codes[(base + t) * CP + k] = (int16_t)plan_code(tab, cnt, P, s0, row, t, k);
     };
     int qn = 0;   // warp-uniform queue length
 #pragma unroll
@@ -304,19 +317,19 @@ __global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P)
     }
     if (lane < qn) resolve(q[lane]);
   } else {
-    for (int i = threadIdx.x; i < kPlanHash / 4; i += kPlanThreads)
-      reinterpret_cast<uint4*>(tab)[i] = make_uint4(kPlanEmpty, kPlanEmpty, kPlanEmpty, kPlanEmpty);
+    for (int i = threadIdx.x; i < kPlanBuckets / 4; i += kPlanThreads)
+      reinterpret_cast<uint4*>(cnt)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     for (int e = threadIdx.x; e < nins; e += kPlanThreads) {
       const int ds = e / W;
-      plan_insert(tab, __ldg(ins + e), P.N, ds, e - ds * W);
+      plan_insert(tab, cnt, __ldg(ins + e), P.N, ds, e - ds * W);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < nlook; e += kPlanThreads) {
       const int dt = e / WR, k = e - dt * WR, t = t0 + dt;
       const int row = k < W ? __ldg(P.idx_w + (base + t) * W + k)
                             : __ldg(P.idx_r + (base + t) * R + (k - W));
-      P.codes[(base + t) * CP + k] = (int16_t)plan_code(tab, P, s0, row, t, k);
+      P.codes[(base + t) * CP + k] = (int16_t)plan_code(tab, cnt, P, s0, row, t, k);
     }
   }
 }

@@ -61,11 +61,11 @@ constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr int kPlanTB = 64;          // steps per plan CTA
 constexpr int kPlanThreads = 512;
 constexpr int kPlanBuckets = 4096;   // hash buckets of 4 entries (uint32) each
-constexpr int kPlanBloom = 2048;     // filter words (65536 bits)
+constexpr int kPlanBloom = 2048;     // words of each filter (65536 bits)
 constexpr int kPlanQCap = 160;       // per-warp queue of filter hits (< 32 + 4 * 32)
-// Shared memory: entries, bucket counts, filter, queues.
+// Shared memory: entries, bucket counts, two filters, queues.
 constexpr size_t kPlanSmem =
-    sizeof(uint32_t) * (5 * kPlanBuckets + kPlanBloom + (kPlanThreads / 32) * kPlanQCap);
+    sizeof(uint32_t) * (5 * kPlanBuckets + 2 * kPlanBloom + (kPlanThreads / 32) * kPlanQCap);
 
 // One step's metadata.  Every array starts on a 16-byte boundary (16-byte
 // cp.async destinations).
@@ -143,8 +143,11 @@ struct PlanArgs {
 __device__ __forceinline__ uint32_t plan_bucket(uint32_t row) {
   return (row * 0x9E3779B1u) >> 20;
 }
-// Filter bit of a row.
-__device__ __forceinline__ uint32_t plan_bit(uint32_t row) { return (row * 0x85EBCA6Bu) >> 16; }
+// Filter bit of a row: the row itself when the table has at most 65536 rows
+// (an exact membership bitmap), else 16 bits of a multiplicative hash.
+__device__ __forceinline__ uint32_t plan_bit(uint32_t row, uint32_t N) {
+  return N <= 65536u ? row : (row * 0x9E3779B1u) >> 16;
+}
 
 // Entry = (row << 13) | (step - s0) << 6 | position; rows < 2^18, step offsets
 // < 128 (kPlanTB + depth - 1), positions < 64.  An insert claims the next
@@ -204,84 +207,82 @@ __device__ __forceinline__ int plan_code(const uint32_t* tab, const uint32_t* cn
   return best >= 0 ? ((t - best) << 6) | bp : -1;
 }
 
-// VEC (W and R multiples of 4): every thread first issues all of its index
-// loads as 16-byte vectors, so the CTA's reads are in flight together.  Rows
-// of the block's write sets also set a bit of a 65536-bit filter; nearly
-// every lookup misses the filter (a step's rows were rarely written in the
-// few steps before it) and gets code -1 at once.  Filter hits, and rows out
-// of range, queue per warp and are resolved 32 at a time on the hash table,
-// so the probe loops run with full warps.
+// VEC (W and R multiples of 4): warp w owns steps w, w + 16, ... of the
+// block and lane l positions 4l .. 4l+3 of a step, so no index needs a
+// division; every thread first issues all of its index loads as 16-byte
+// vectors.  Rows of the block's write sets also mark two 65536-bit filters,
+// "written once" and "written again", so a read lookup that misses the first
+// or a write lookup that misses the second (its own insert set the first)
+// cannot have an earlier writer in the window and gets code -1 at once --
+// nearly every lookup.  Filter hits queue per warp and are resolved 32 at a
+// time on the hash table, so the probe loops run with full warps.
 template <bool VEC>
 __global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P) {
   extern __shared__ __align__(16) uint32_t tab[];
   uint32_t* cnt = tab + 4 * kPlanBuckets;
-  uint32_t* bloom = cnt + kPlanBuckets;
+  uint32_t* once = cnt + kPlanBuckets;
+  uint32_t* again = once + kPlanBloom;
   const int chain = blockIdx.y;
   const int t0 = blockIdx.x * kPlanTB;
   const int t1 = min(P.T, t0 + kPlanTB);
   const int s0 = max(0, t0 - (P.depth - 1));
   const int W = P.W, R = P.R, WR = W + R, CP = code_pitch(W, R);
   const size_t base = (size_t)chain * P.T;
-  const int nins = (t1 - s0) * W;          // write slots of steps s0 .. t1-1, contiguous
-  const int nlook = (t1 - t0) * WR;
-  const int32_t* ins = P.idx_w + (base + s0) * W;
   if constexpr (VEC) {
-    // Groups of 4 consecutive positions never straddle the write/read boundary.
-    constexpr int kIns = ((kPlanTB + 15) * 64 / 4 + kPlanThreads - 1) / kPlanThreads;
-    constexpr int kLook = kPlanTB * 128 / 4 / kPlanThreads;
-    const int lane = threadIdx.x & 31;
-    uint32_t* q = bloom + kPlanBloom + (threadIdx.x >> 5) * kPlanQCap;
+    constexpr int kWarps = kPlanThreads / 32;
+    constexpr int kLook = kPlanTB / kWarps;                        // steps per warp
+    constexpr int kIns = (kPlanTB + 15 + kWarps - 1) / kWarps;     // insert steps per warp
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int k = 4 * lane;
+    const bool lk = k < WR, lw = k < W;
+    const int32_t* iw = P.idx_w + base * W;
+    const int32_t* ir = P.idx_r + base * R;
+    int16_t* cb = P.codes + base * CP;
+    uint32_t* q = again + kPlanBloom + warp * kPlanQCap;
     int4 look[kLook], irow[kIns];
 #pragma unroll
     for (int i = 0; i < kLook; ++i) {
-      const int g = 4 * (threadIdx.x + i * kPlanThreads);
-      if (g < nlook) {
-        const int dt = g / WR, k = g - dt * WR, t = t0 + dt;
-        const int32_t* src = k < W ? P.idx_w + (base + t) * W + k : P.idx_r + (base + t) * R + (k - W);
-        look[i] = __ldg(reinterpret_cast<const int4*>(src));
-      }
+      const int t = t0 + warp + kWarps * i;
+      if (t < t1 && lk)
+        look[i] = __ldg(reinterpret_cast<const int4*>(lw ? iw + (size_t)t * W + k
+                                                         : ir + (size_t)t * R + (k - W)));
     }
 #pragma unroll
     for (int i = 0; i < kIns; ++i) {
-      const int g = 4 * (threadIdx.x + i * kPlanThreads);
-      if (g < nins) irow[i] = __ldg(reinterpret_cast<const int4*>(ins + g));
+      const int s = s0 + warp + kWarps * i;
+      if (s < t1 && lw) irow[i] = __ldg(reinterpret_cast<const int4*>(iw + (size_t)s * W + k));
     }
-    // Counts and filter are adjacent: one clear (entries need none).
-    for (int i = threadIdx.x; i < (kPlanBuckets + kPlanBloom) / 4; i += kPlanThreads)
+    // Counts and filters are adjacent: one clear (entries need none).
+    for (int i = threadIdx.x; i < (kPlanBuckets + 2 * kPlanBloom) / 4; i += kPlanThreads)
       reinterpret_cast<uint4*>(cnt)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kIns; ++i) {
-      const int g = 4 * (threadIdx.x + i * kPlanThreads);
-      if (g < nins) {
-        const int ds = g / W, j = g - ds * W;
+      const int ds = warp + kWarps * i;
+      if (s0 + ds < t1 && lw) {
         const int r4[4] = {irow[i].x, irow[i].y, irow[i].z, irow[i].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if (r4[e] < 0 || (uint32_t)r4[e] >= P.N) continue;
-          const uint32_t hb = plan_bit((uint32_t)r4[e]);
-          atomicOr(&bloom[hb >> 5], 1u << (hb & 31u));
-          plan_insert(tab, cnt, r4[e], P.N, ds, j + e);
+          const uint32_t hb = plan_bit((uint32_t)r4[e], P.N), m = 1u << (hb & 31u);
+          if (atomicOr(&once[hb >> 5], m) & m) atomicOr(&again[hb >> 5], m);
+          plan_insert(tab, cnt, r4[e], P.N, ds, k + e);
         }
       }
     }
     __syncthreads();
-    // Resolve queued hits: entry = (row << 13) | (dt * WR + k).
+    // Queued hit: (row << 13) | (dt << 7) | position.
     auto resolve = [&](uint32_t ent) {
-      const int row = (int)(ent >> 13), pos = (int)(ent & 8191u);
-      const int dt = pos / WR, k = pos - dt * WR, t = t0 + dt;
-      P.codes[(base + t) * CP + k] = (int16_t)plan_code(tab, cnt, P, s0, row, t, k);
+      const int t = t0 + (int)((ent >> 7) & 63u), kk = (int)(ent & 127u);
+      cb[(size_t)t * CP + kk] = (int16_t)plan_code(tab, cnt, P, s0, (int)(ent >> 13), t, kk);
     };
     int qn = 0;   // warp-uniform queue length
 #pragma unroll
     for (int i = 0; i < kLook; ++i) {
-      const int g = 4 * (threadIdx.x + i * kPlanThreads);
+      const int dt = warp + kWarps * i, t = t0 + dt;
       uint32_t hit = 0;
-      int dt = 0, k = 0;
       const int r4[4] = {look[i].x, look[i].y, look[i].z, look[i].w};
-      if (g < nlook) {
-        dt = g / WR;
-        k = g - dt * WR;
+      if (t < t1 && lk) {
         uint32_t c16[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -290,13 +291,13 @@ __global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P)
             record_status(P.status, SDM_ERR_DEVICE_BOUNDS);
             c16[e] = 0xfffeu;                  // -2: invalid
           } else {
-            const uint32_t hb = plan_bit((uint32_t)r4[e]);
-            hit |= ((bloom[hb >> 5] >> (hb & 31u)) & 1u) << e;
+            const uint32_t hb = plan_bit((uint32_t)r4[e], P.N);
+            hit |= (((lw ? again : once)[hb >> 5] >> (hb & 31u)) & 1u) << e;
           }
         }
         // Hits are overwritten after the warp barrier below.  CP is a
         // multiple of 8 and k of 4: one aligned 8-byte store.
-        *reinterpret_cast<uint2*>(P.codes + (base + t0 + dt) * CP + k) =
+        *reinterpret_cast<uint2*>(cb + (size_t)t * CP + k) =
             make_uint2(c16[0] | (c16[1] << 16), c16[2] | (c16[3] << 16));
       }
 #pragma unroll
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P)
         const unsigned bal = __ballot_sync(0xffffffffu, h);
         if (h)
           q[qn + __popc(bal & ((1u << lane) - 1u))] =
-              ((uint32_t)r4[e] << 13) | (uint32_t)(dt * WR + k + e);
+              ((uint32_t)r4[e] << 13) | ((uint32_t)dt << 7) | (uint32_t)(k + e);
         qn += __popc(bal);
       }
       __syncwarp();
@@ -317,6 +318,9 @@ __global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P)
     }
     if (lane < qn) resolve(q[lane]);
   } else {
+    const int nins = (t1 - s0) * W;        // write slots of steps s0 .. t1-1, contiguous
+    const int nlook = (t1 - t0) * WR;
+    const int32_t* ins = P.idx_w + (base + s0) * W;
     for (int i = threadIdx.x; i < kPlanBuckets / 4; i += kPlanThreads)
       reinterpret_cast<uint4*>(cnt)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();

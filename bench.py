@@ -348,9 +348,10 @@ def run_ours(args, w):
 
         # ---- end to end through the public API with host buffers: every
         # step copies its inputs from pinned host memory and its y back.  The
-        # copies run on a second stream, double-buffered, so step i's compute
-        # overlaps step i+1's upload and step i-1's download (the table is
-        # carried in place, in order, on the compute stream).
+        # copies run on two more streams (uploads, read-backs), double-
+        # buffered, so step i's compute overlaps step i+1's upload and step
+        # i-1's read-back (the table is carried in place, in order, on the
+        # compute stream).
         names = ("q_w", "q_r", "alpha", "beta", "v")
         host = {k: g[k].cpu().pin_memory() for k in names}
         bufs = [{k: torch.empty_like(g[k]) for k in names} for _ in range(2)]
@@ -359,7 +360,10 @@ def run_ours(args, w):
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = y_host[0].numel() * y_host[0].element_size()
         ne = max(4, min(args.steps, 20))
+        # Uploads and read-backs on streams of their own: the two directions
+        # overlap each other as well as the compute.
         copy = torch.cuda.Stream(dev)
+        copy_back = torch.cuda.Stream(dev)
         g_keep = dict(g)
 
         def run_e2e(n):
@@ -376,10 +380,10 @@ def run_ours(args, w):
                         up[i].record(copy)
                 if i >= 1:
                     j = i - 1
-                    with torch.cuda.stream(copy):
-                        copy.wait_event(done[j])
+                    with torch.cuda.stream(copy_back):
+                        copy_back.wait_event(done[j])
                         y_host[j % 2].copy_(y_dev[j % 2], non_blocking=True)
-                        down[j].record(copy)
+                        down[j].record(copy_back)
                 if i < n:
                     stream.wait_event(up[i])
                     if i >= 2:
@@ -441,6 +445,7 @@ def run_ours(args, w):
             a, b = ev(), ev()
             a.record(stream)
             copy.wait_event(a)                     # no upload starts before the timed region
+            copy_back.wait_event(a)
             last = run_e2e(ne)
             stream.wait_event(last)
             b.record(stream)

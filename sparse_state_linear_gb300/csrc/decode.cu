@@ -9,8 +9,11 @@
 //
 // A decode step has little work per chain but a long dependent path
 // (scores -> top-k -> merge -> write -> read), so the tile kernels used for
-// long sequences spend most of it waiting.  Here one CTA owns one (b, h)
-// chain and runs its T steps in order, each step entirely on chip:
+// long sequences spend most of it waiting.  Here P CTAs own one (b, h)
+// chain, each a 1/P range of its columns (P > 1 when there are too few
+// chains to fill the GPU: the write and read act column by column, so the
+// parts share nothing but the selection, which each part computes itself),
+// and run its T steps in order, each step entirely on chip:
 //   scores    FFMA (or inverse distance) of the four half-queries against
 //             the two sub-key tables, into shared memory;
 //   top-k     warps 0-3, one half-row each (select.cuh, exact);
@@ -22,7 +25,9 @@
 //   read      after a block barrier (the CTA's own global writes are then
 //             visible to all its threads) the R read rows, batched the same
 //             way; optionally the RMS-Norm + gate epilogue, whose row sum of
-//             squares is a block reduction because the whole row is here.
+//             squares is a block reduction, plus, for P > 1, a sum of the
+//             parts' shares over distributed shared memory (the P CTAs of a
+//             chain are one thread-block cluster).
 // The table is read with plain (coherent) loads: the CTA rewrites it.
 #include "common.cuh"
 #include "internal.h"
@@ -55,6 +60,7 @@ struct DecArgs {
   void* out;            // epilogue output or null (no epilogue)
   float eps;
   int out_dtype;
+  int P;                // CTAs (column parts) per chain; a cluster when out != null
 };
 
 struct DecLayout {
@@ -74,7 +80,7 @@ __host__ __device__ inline DecLayout dec_layout(int s, int dh) {
   L.stair = o; o = dl_align(o + sizeof(uint16_t) * 2 * kStairCap);
   L.nst = o;   o = dl_align(o + sizeof(int) * 2);
   L.sel = o;   o = dl_align(o + sizeof(float) * 4 * kMaxSel);   // idx_w, wt_w, idx_r, wt_r
-  L.red = o;   o = dl_align(o + sizeof(float) * kDecWarps);
+  L.red = o;   o = dl_align(o + sizeof(float) * (kDecWarps + 1));   // + this part's share
   L.part = o;  o = dl_align(o + sizeof(float) * 4 * kDecThreads);   // row-group partials
   L.total = o;
   return L;
@@ -156,14 +162,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
   float4* part = reinterpret_cast<float4*>(smem + L.part);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int chain = blockIdx.x;              // b * H + h
+  const int chain = blockIdx.x / A.P;        // b * H + h
+  const int cpart = blockIdx.x - chain * A.P; // column part = rank in the chain's cluster
   const int h = chain % d.H;
   const int s = d.s, dh = d.dh, dv = d.dv, W = d.W, R = d.R;
-  const int nc4 = dv / 4;
+  const int nc4 = dv / 4, ncp = nc4 / A.P;   // 16-byte chunks of a row, of this part
   // Write / read work items: (column chunk c4, row group rg); the G row
   // groups of a chunk split its rows and combine partial sums on chip.
-  const int G = kDecThreads / nc4;           // >= 1 (d_v <= 2048)
-  const int c4 = tid % nc4, rg = tid / nc4;
+  const int G = kDecThreads / ncp;           // >= 1 (d_v <= 2048)
+  const int lc = tid % ncp, rg = tid / ncp;
+  const int c4 = cpart * ncp + lc;
   const bool worker = rg < G;
   float* Mc = A.M + (size_t)chain * (size_t)d.N() * dv;
   const bool fig2 = d.update == SDM_UPDATE_SHARED_RESIDUAL;
@@ -245,10 +253,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
       __syncwarp();
       int32_t* io = (sg == 0 ? A.idx_w : A.idx_r) + th * nsel;
       float* wo = (sg == 0 ? A.wt_w : A.wt_r) + th * nsel;
-      for (int e = lane; e < nsel; e += 32) {
-        io[e] = sidx[sg * kMaxSel + e];
-        wo[e] = swt[sg * kMaxSel + e];
-      }
+      if (cpart == 0)
+        for (int e = lane; e < nsel; e += 32) {
+          io[e] = sidx[sg * kMaxSel + e];
+          wo[e] = swt[sg * kMaxSel + e];
+        }
     }
     __syncthreads();
 
@@ -280,13 +289,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
               vh.w = fmaf(wj, a * x[u].w, vh.w);
             }
         }
-        part[rg * nc4 + c4] = vh;
+        part[rg * ncp + lc] = vh;
       }
       __syncthreads();
       if (worker) {
-        vh = part[c4];
+        vh = part[lc];
         for (int g2 = 1; g2 < G; ++g2) {
-          const float4 p2 = part[g2 * nc4 + c4];
+          const float4 p2 = part[g2 * ncp + lc];
           vh.x += p2.x;
           vh.y += p2.y;
           vh.z += p2.z;
@@ -347,15 +356,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
             acc.w = fmaf(w, x[u].w, acc.w);
           }
       }
-      part[rg * nc4 + c4] = acc;
+      part[rg * ncp + lc] = acc;
     }
     __syncthreads();
     float4 yv = make_float4(0.f, 0.f, 0.f, 0.f);
     float ss = 0.f;
     if (rg == 0) {
-      yv = part[c4];
+      yv = part[lc];
       for (int g2 = 1; g2 < G; ++g2) {
-        const float4 p2 = part[g2 * nc4 + c4];
+        const float4 p2 = part[g2 * ncp + lc];
         yv.x += p2.x;
         yv.y += p2.y;
         yv.z += p2.z;
@@ -375,6 +384,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
       float tot = 0.f;
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) tot += red[w];
+      if (A.P > 1) {
+        // Sum the parts' shares: each part publishes its own, the cluster
+        // barrier orders them, every thread reads all P from distributed
+        // shared memory, and a second barrier keeps each share in place
+        // until every part has read it.
+        if (tid == 0) red[kDecWarps] = tot;
+        cluster_sync();
+        tot = 0.f;
+        const uint32_t mine = smem_u32(red + kDecWarps);
+        for (int r = 0; r < A.P; ++r) tot += ld_cluster_f32(map_cluster(mine, (uint32_t)r));
+        cluster_sync();
+      }
       const float inv = 1.f / sqrtf(tot / (float)dv + A.eps);
       if (rg == 0) {
         const float4 gt = ld_in4<BF16>(A.g, th * nc4 + c4);
@@ -397,7 +418,26 @@ cudaError_t launch_dec(const DecArgs& A, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kfn<<<(unsigned)(A.d.B * A.d.H), kDecThreads, smem, stream>>>(A);
+  const unsigned grid = (unsigned)(A.d.B * A.d.H * A.P);
+  if (A.P > 1 && A.out) {
+    // The epilogue's row norm spans the parts: they launch as one cluster.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)A.P;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kfn, A);
+    if (e != cudaSuccess) return e;
+  } else {
+    kfn<<<grid, kDecThreads, smem, stream>>>(A);
+  }
   return cudaGetLastError();
 }
 
@@ -418,9 +458,18 @@ cudaError_t launch_decode(const Dims& d, const void* q_w, const void* q_r, const
                           int32_t* idx_w, float* wt_w, int32_t* idx_r, float* wt_r,
                           const void* g, const float* gamma, float eps, void* out,
                           int out_dtype, cudaStream_t stream) {
-  if ((long long)d.B * d.H == 0 || d.T == 0) return cudaSuccess;
+  const long long chains = (long long)d.B * d.H;
+  if (chains == 0 || d.T == 0) return cudaSuccess;
+  // Column parts per chain: as many as keep one CTA per SM busy (a CTA of
+  // 512 threads at up to 128 registers is alone on its SM), each part at
+  // least 32 chunks of 16 bytes wide.
+  constexpr int kSMs = 152;
+  const int nc4 = d.dv / 4;
+  int P = 1;
+  for (int p = 2; p <= 8; p *= 2)
+    if (chains * p <= kSMs && nc4 % p == 0 && nc4 / p >= 32) P = p;
   DecArgs A{d, q_w, q_r, K, alpha, beta, v, M, y, idx_w, wt_w, idx_r, wt_r,
-            g, gamma, out, eps, out_dtype};
+            g, gamma, out, eps, out_dtype, P};
   return d.s <= 256 ? launch_pl<8>(A, stream) : launch_pl<16>(A, stream);
 }
 

@@ -64,7 +64,7 @@ struct DecArgs {
 };
 
 struct DecLayout {
-  size_t q, S, lv, lid, ws, stair, nst, sel, red, part, total;
+  size_t q, S, lv, lid, ws, gs, stair, nst, sel, red, part, total;
 };
 
 __host__ __device__ inline size_t dl_align(size_t x) { return (x + 15) / 16 * 16; }
@@ -77,6 +77,7 @@ __host__ __device__ inline DecLayout dec_layout(int s, int dh) {
   L.lv = o;    o = dl_align(o + sizeof(float) * 4 * kMaxSel);
   L.lid = o;   o = dl_align(o + sizeof(uint32_t) * 4 * kMaxSel);
   L.ws = o;    o = dl_align(o + sizeof(WarpScratch) * 4);
+  L.gs = o;    o = dl_align(o + sizeof(GroupScratch) * 4);
   L.stair = o; o = dl_align(o + sizeof(uint16_t) * 2 * kStairCap);
   L.nst = o;   o = dl_align(o + sizeof(int) * 2);
   L.sel = o;   o = dl_align(o + sizeof(float) * 4 * kMaxSel);   // idx_w, wt_w, idx_r, wt_r
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
   float* lv = reinterpret_cast<float*>(smem + L.lv);
   uint32_t* lid = reinterpret_cast<uint32_t*>(smem + L.lid);
   WarpScratch* wsa = reinterpret_cast<WarpScratch*>(smem + L.ws);
+  GroupScratch* gsa = reinterpret_cast<GroupScratch*>(smem + L.gs);
   uint16_t* stair = reinterpret_cast<uint16_t*>(smem + L.stair);
   int* nst = reinterpret_cast<int*>(smem + L.nst);
   int32_t* sidx = reinterpret_cast<int32_t*>(smem + L.sel);      // [2][64]
@@ -201,63 +203,115 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs A)
     }
     __syncthreads();
     // ---- sub-scores S[(sigma * 2 + p) * s + j]: one thread per (p, j) loads
-    // sub-key K_p[j] once, 16 elements at a time with every load of a chunk
-    // in flight, and scores it against both branches' half-queries.
+    // sub-key K_p[j] once -- for d_h = 64 in bf16 the whole row in one round
+    // trip -- and scores it against both branches' half-queries (read from
+    // shared memory four floats at a time).
     for (int e = tid; e < 2 * s; e += kDecThreads) {
       const int p = e / s, j = e - p * s;
       const float* qw = qs + p * dh;           // write branch, half p
       const float* qr = qs + (2 + p) * dh;     // read branch, half p
       const size_t kb = ((size_t)(h * 2 + p) * s + j) * dh;
       float aw = 0.f, ar = 0.f;
-#pragma unroll 2
-      for (int c0 = 0; c0 < dh; c0 += 16) {
-        float k[16];
-        ld_in16<BF16>(A.K, kb + c0, k);
+      auto acc16 = [&](int c0, const float (&k)[16]) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (KIND == SDM_SCORE_DOT) {
-            aw = fmaf(qw[c0 + i], k[i], aw);
-            ar = fmaf(qr[c0 + i], k[i], ar);
-          } else {
-            const float dw = qw[c0 + i] - k[i], dr = qr[c0 + i] - k[i];
-            aw = fmaf(dw, dw, aw);
-            ar = fmaf(dr, dr, ar);
+        for (int i = 0; i < 16; i += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(qw + c0 + i);
+          const float4 r4 = *reinterpret_cast<const float4*>(qr + c0 + i);
+          const float wq[4] = {w4.x, w4.y, w4.z, w4.w}, rq[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (KIND == SDM_SCORE_DOT) {
+              aw = fmaf(wq[u], k[i + u], aw);
+              ar = fmaf(rq[u], k[i + u], ar);
+            } else {
+              const float dw = wq[u] - k[i + u], dr = rq[u] - k[i + u];
+              aw = fmaf(dw, dw, aw);
+              ar = fmaf(dr, dr, ar);
+            }
           }
+        }
+      };
+      if (BF16 && dh == 64) {
+        float k0[16], k1[16], k2[16], k3[16];
+        ld_in16<BF16>(A.K, kb, k0);
+        ld_in16<BF16>(A.K, kb + 16, k1);
+        ld_in16<BF16>(A.K, kb + 32, k2);
+        ld_in16<BF16>(A.K, kb + 48, k3);
+        acc16(0, k0);
+        acc16(16, k1);
+        acc16(32, k2);
+        acc16(48, k3);
+      } else {
+#pragma unroll 2
+        for (int c0 = 0; c0 < dh; c0 += 16) {
+          float k[16];
+          ld_in16<BF16>(A.K, kb + c0, k);
+          acc16(c0, k);
         }
       }
       S[p * s + j] = KIND == SDM_SCORE_DOT ? aw : -logf(d.eps + aw);
       S[(2 + p) * s + j] = KIND == SDM_SCORE_DOT ? ar : -logf(d.eps + ar);
     }
     __syncthreads();
-    // ---- per-half top-k: warp w < 4 takes half-row w = sigma * 2 + p
-    if (warp < 4) {
-      const int k = (warp >> 1) == 0 ? d.kw : d.kr;
-      WarpScratch& ws = wsa[warp];
-      RowSrc src{S + warp * s};
-      warp_topk<PL>(src, s, k, ws, lane);
-      for (int e = lane; e < k; e += 32) {
-        lv[warp * kMaxSel + e] = ws.out_v[e];
-        lid[warp * kMaxSel + e] = ws.out_id[e];
+    // ---- per-half top-k: warps 4g .. 4g+3 take half-row g = sigma * 2 + p
+    // together (named barrier 1 + g); the warp paths remain for the rows the
+    // buckets cannot decide.
+    {
+      const int g = warp >> 2, gt = tid & 127;
+      const int k = (g >> 1) == 0 ? d.kw : d.kr;
+      RowSrc src{S + g * s};
+      const float* ov = gsa[g].out_v;
+      const uint32_t* oi = gsa[g].out_id;
+      if (!group_topk_bucketed<4, PL / 4>(src, s, k, gsa[g], gt, 1 + g)) {
+        if ((warp & 3) == 0) warp_topk_sorted(src, s, k, wsa[g], lane);
+        named_bar_sync(1 + g, 128);
+        ov = wsa[g].out_v;
+        oi = wsa[g].out_id;
+      }
+      for (int e = gt; e < k; e += 128) {
+        lv[g * kMaxSel + e] = ov[e];
+        lid[g * kMaxSel + e] = oi[e];
       }
     }
     __syncthreads();
-    // ---- merge + softmax: warp sigma < 2
-    if (warp < 2) {
-      const int sg = warp;
+    // ---- merge + softmax: warps 8 sigma .. 8 sigma + 7 rank the staircase
+    // pairs of branch sigma together (named barrier 5 + sigma); a tie at the
+    // W-th sum, or rows the buckets cannot decide, take the warp merge.
+    {
+      const int sg = warp >> 3, gt = tid & 255;
       const int k = sg == 0 ? d.kw : d.kr, nsel = sg == 0 ? W : R;
-      WarpScratch& ws = wsa[sg];
-      warp_merge(lv + (2 * sg) * kMaxSel, lid + (2 * sg) * kMaxSel, lv + (2 * sg + 1) * kMaxSel,
-                 lid + (2 * sg + 1) * kMaxSel, k, nsel, (uint32_t)s, stair + sg * kStairCap,
-                 nst[sg], ws, lane);
-      warp_softmax_store(ws, nsel, sidx + sg * kMaxSel, swt + sg * kMaxSel, lane);
-      __syncwarp();
-      int32_t* io = (sg == 0 ? A.idx_w : A.idx_r) + th * nsel;
-      float* wo = (sg == 0 ? A.wt_w : A.wt_r) + th * nsel;
-      if (cpart == 0)
-        for (int e = lane; e < nsel; e += 32) {
-          io[e] = sidx[sg * kMaxSel + e];
-          wo[e] = swt[sg * kMaxSel + e];
+      const float* v1 = lv + (2 * sg) * kMaxSel;
+      const uint32_t* i1 = lid + (2 * sg) * kMaxSel;
+      const float* v2 = lv + (2 * sg + 1) * kMaxSel;
+      const uint32_t* i2 = lid + (2 * sg + 1) * kMaxSel;
+      GroupScratch& gs = gsa[sg];
+      PairSrc ps{v1, i1, v2, i2, stair + sg * kStairCap, (uint32_t)s};
+      bool ok = group_topk_bucketed<8, 2>(ps, nst[sg], nsel, gs, gt, 5 + sg);
+      bool tie = false;
+      if (ok && gt < k) {
+        const int b = nsel / (gt + 1);
+        tie = b < k && __fadd_rn(v1[gt], v2[b]) >= gs.out_v[nsel - 1];
+      }
+      ok = !named_bar_or(5 + sg, 256, !ok || tie);
+      if ((warp & 7) == 0) {
+        const float* ov = gs.out_v;
+        const uint32_t* oi = gs.out_id;
+        if (!ok) {
+          warp_merge(v1, i1, v2, i2, k, nsel, (uint32_t)s, stair + sg * kStairCap, nst[sg],
+                     wsa[sg], lane);
+          ov = wsa[sg].out_v;
+          oi = wsa[sg].out_id;
         }
+        softmax_store(ov, oi, nsel, sidx + sg * kMaxSel, swt + sg * kMaxSel, lane);
+        __syncwarp();
+        int32_t* io = (sg == 0 ? A.idx_w : A.idx_r) + th * nsel;
+        float* wo = (sg == 0 ? A.wt_w : A.wt_r) + th * nsel;
+        if (cpart == 0)
+          for (int e = lane; e < nsel; e += 32) {
+            io[e] = sidx[sg * kMaxSel + e];
+            wo[e] = swt[sg * kMaxSel + e];
+          }
+      }
     }
     __syncthreads();
 

@@ -465,24 +465,158 @@ __device__ __forceinline__ void warp_merge(const float* v1, const uint32_t* id1,
   }
 }
 
-// Softmax of ws.out_v[0..nsel) and store of slots and weights (best first).
-__device__ __forceinline__ void warp_softmax_store(const WarpScratch& ws, int nsel,
-                                                   int32_t* idx_out, float* wt_out,
-                                                   int lane) {
-  const float m = ws.out_v[0];
-  const float e0 = lane < nsel ? expf(ws.out_v[lane] - m) : 0.f;
-  const float e1 = lane + 32 < nsel ? expf(ws.out_v[lane + 32] - m) : 0.f;
+// Softmax of ov[0..nsel) and store of slots oi and weights (best first).
+__device__ __forceinline__ void softmax_store(const float* ov, const uint32_t* oi, int nsel,
+                                              int32_t* idx_out, float* wt_out, int lane) {
+  const float m = ov[0];
+  const float e0 = lane < nsel ? expf(ov[lane] - m) : 0.f;
+  const float e1 = lane + 32 < nsel ? expf(ov[lane + 32] - m) : 0.f;
   float sum = e0 + e1;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
   if (lane < nsel) {
-    idx_out[lane] = (int32_t)ws.out_id[lane];
+    idx_out[lane] = (int32_t)oi[lane];
     wt_out[lane] = e0 / sum;
   }
   if (lane + 32 < nsel) {
-    idx_out[lane + 32] = (int32_t)ws.out_id[lane + 32];
+    idx_out[lane + 32] = (int32_t)oi[lane + 32];
     wt_out[lane + 32] = e1 / sum;
   }
+}
+__device__ __forceinline__ void warp_softmax_store(const WarpScratch& ws, int nsel,
+                                                   int32_t* idx_out, float* wt_out,
+                                                   int lane) {
+  softmax_store(ws.out_v, ws.out_id, nsel, idx_out, wt_out, lane);
+}
+
+// ------------------------------------------------------------ warp groups
+// The bucketed top-k above, shared by a group of NW consecutive warps that
+// synchronise on named barrier `bar` (for latency-bound callers with idle
+// warps: each phase then touches PL elements per thread instead of a warp's
+// n / 32).  Same buckets, same exact ranks, so the same result as
+// warp_topk_bucketed; returns false (group-uniform, nothing written) where
+// that one would, and the caller falls back to the warp paths.
+constexpr int kGTmpCap = 256;
+
+struct GroupScratch {
+  uint32_t hist[256];          // bucket counts, then scatter cursors
+  uint32_t base[260];          // exclusive prefix of the counts
+  float tmp_v[kGTmpCap];       // candidates in bucket order
+  uint32_t tmp_id[kGTmpCap];
+  float out_v[kMaxSel];
+  uint32_t out_id[kMaxSel];
+  float wmin[8], wmax[8];      // per-warp extremes
+  uint32_t wsum[8];            // per-warp bucket totals (prefix scan)
+  uint32_t bstar;
+};
+
+template <int NW, int PL, class Src>
+__device__ bool group_topk_bucketed(const Src& src, int n, int k, GroupScratch& g, int gt,
+                                    int bar) {
+  constexpr int NT = 32 * NW;
+  constexpr int BPT = 256 / NT;    // buckets per thread in the prefix scan
+  static_assert(NT <= 256 && 256 % NT == 0, "group size");
+  const int lane = gt & 31, w = gt >> 5;
+  float v[PL];
+  uint32_t id[PL];
+  float vmax = -INFINITY, vmin = INFINITY;
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const int e = gt + NT * i;
+    v[i] = 0.f;
+    id[i] = 0u;
+    if (e < n) {
+      src.get(e, v[i], id[i]);
+      vmax = fmaxf(vmax, v[i]);
+      vmin = fminf(vmin, v[i]);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, off));
+    vmin = fminf(vmin, __shfl_xor_sync(kFull, vmin, off));
+  }
+  if (lane == 0) {
+    g.wmax[w] = vmax;
+    g.wmin[w] = vmin;
+  }
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) g.hist[gt * BPT + i] = 0u;
+  named_bar_sync(bar, NT);
+  vmax = g.wmax[0];
+  vmin = g.wmin[0];
+#pragma unroll
+  for (int i = 1; i < NW; ++i) {
+    vmax = fmaxf(vmax, g.wmax[i]);
+    vmin = fminf(vmin, g.wmin[i]);
+  }
+  const float range = vmax - vmin;
+  if (!(range > 0.f) || !(range < INFINITY)) return false;
+  const float scale = 256.f / range;
+  auto bucket = [&](float x) -> uint32_t {
+    const float dd = (vmax - x) * scale;
+    return min(255u, __float2uint_rz(dd));
+  };
+#pragma unroll
+  for (int i = 0; i < PL; ++i)
+    if (gt + NT * i < n) atomicAdd(&g.hist[bucket(v[i])], 1u);
+  named_bar_sync(bar, NT);
+  // Exclusive prefix over the buckets: thread gt owns BPT consecutive ones.
+  uint32_t c[BPT], tot = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    c[i] = g.hist[gt * BPT + i];
+    tot += c[i];
+  }
+  uint32_t inc = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(kFull, inc, off);
+    if (lane >= off) inc += t;
+  }
+  if (lane == 31) g.wsum[w] = inc;
+  named_bar_sync(bar, NT);
+  uint32_t run = inc - tot;
+  for (int i = 0; i < w; ++i) run += g.wsum[i];
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    const int b = gt * BPT + i;
+    if (run < (uint32_t)k && (uint32_t)k <= run + c[i]) g.bstar = (uint32_t)b;
+    g.base[b] = run;
+    g.hist[b] = run;             // scatter cursor
+    run += c[i];
+  }
+  if (gt == NT - 1) g.base[256] = run;
+  named_bar_sync(bar, NT);
+  const uint32_t bstar = g.bstar;
+  const uint32_t ncand = g.base[bstar + 1];
+  if (ncand > (uint32_t)kGTmpCap) return false;
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    if (gt + NT * i < n) {
+      const uint32_t b = bucket(v[i]);
+      if (b <= bstar) {
+        const uint32_t pos = atomicAdd(&g.hist[b], 1u);
+        g.tmp_v[pos] = v[i];
+        g.tmp_id[pos] = id[i];
+      }
+    }
+  }
+  named_bar_sync(bar, NT);
+  for (uint32_t p = gt; p < ncand; p += NT) {
+    const float pv = g.tmp_v[p];
+    const uint32_t pid = g.tmp_id[p];
+    const uint32_t b = bucket(pv);
+    const uint32_t lo = g.base[b], hi = g.base[b + 1];
+    uint32_t r = lo;
+    for (uint32_t q = lo; q < hi; ++q) r += better(g.tmp_v[q], g.tmp_id[q], pv, pid) ? 1u : 0u;
+    if (r < (uint32_t)k) {
+      g.out_v[r] = pv;
+      g.out_id[r] = pid;
+    }
+  }
+  named_bar_sync(bar, NT);
+  return true;
 }
 
 }  // namespace sdm

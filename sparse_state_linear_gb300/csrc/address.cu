@@ -327,7 +327,7 @@ constexpr int kTcRows = 128;
 constexpr int kTcThreads = 1024;
 
 struct TcLayout {
-  size_t a, b, sc, lv, lid, ws, stair, nst, bar, tslot, total;
+  size_t a, b, sc, lv, lid, ws, stair, nst, bar, tslot, th, cut, total;
   int spad, scs;
 };
 
@@ -351,13 +351,15 @@ __host__ __device__ inline TcLayout tc_layout(int s, int dh) {
   L.nst = o;   o = align_up(o + sizeof(int) * 2, 16);
   L.bar = o;   o = align_up(o + sizeof(uint64_t), 16);
   L.tslot = o; o = align_up(o + sizeof(uint32_t), 16);
+  L.th = o;    o = align_up(o + sizeof(long long) * kTcRows, 16);   // row -> token-head, -1 past the end
+  L.cut = o;   o = align_up(o + sizeof(int) * 2 * kMaxSel, 16);     // nsel / (a + 1) per branch
   L.total = o;
   return L;
 }
 
 inline bool tc_eligible(const Dims& d) {
   return d.in_dtype == SDM_BF16 && d.score == SDM_SCORE_DOT && d.s <= 256 && d.dh <= 64 &&
-         d.dh % 16 == 0 && tc_layout(d.s, d.dh).total <= 232448;
+         d.dh % 16 == 0 && (d.dh & (d.dh - 1)) == 0 && tc_layout(d.s, d.dh).total <= 232448;
 }
 
 template <int MODE>
@@ -386,6 +388,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
   int* nst = reinterpret_cast<int*>(smem + L.nst);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L.tslot);
+  long long* rth = reinterpret_cast<long long*>(smem + L.th);
+  int* cut = reinterpret_cast<int*>(smem + L.cut);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.y, dh = d.dh, spad = L.spad, scs = L.scs;
@@ -406,26 +410,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
       if (lane == 0) nst[1] = n;
     }
   }
-  // Operands into the K-major core-matrix layout (16-byte chunks).
-  const int kc = dh / 8;
-  for (int e = tid; e < 2 * kTcRows * kc; e += kTcThreads) {
-    const int p = e / (kTcRows * kc), rem = e - p * kTcRows * kc;
-    const int r = rem / kc, c = rem - r * kc;
+  // Token-head of every MMA row (one 64-bit division per row, here only),
+  // and the staircase's first excluded b per a for the merge's tie check.
+  if (tid < kTcRows) {
     int sg;
     long long item;
-    tc_row_item<MODE>(r, sg, item);
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    tc_row_item<MODE>(tid, sg, item);
+    long long th = -1;
     if (item < BT) {
       const long long b = item / d.T, t = item - b * d.T;
-      const long long th = (b * d.H + h) * d.T + t;
-      const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(sg == 0 ? A.q0 : A.q1);
+      th = (b * d.H + h) * d.T + t;
+    }
+    rth[tid] = th;
+  } else if (tid < kTcRows + 2 * kMaxSel) {
+    const int a = tid - kTcRows;
+    const int nsel = a < kMaxSel ? d.W : d.R;
+    cut[a] = nsel / ((a & (kMaxSel - 1)) + 1);
+  }
+  __syncthreads();
+  // Operands into the K-major core-matrix layout (16-byte chunks); d_h is a
+  // power of two here, so the chunk index splits by shifts.
+  const int kc = dh / 8, lkc = 31 - __clz(kc);
+  for (int e = tid; e < 2 * kTcRows * kc; e += kTcThreads) {
+    const int p = e >> (7 + lkc), rem = e & ((kTcRows << lkc) - 1);
+    const int r = rem >> lkc, c = rem & (kc - 1);
+    const long long th = rth[r];
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (th >= 0) {
+      const __nv_bfloat16* q =
+          reinterpret_cast<const __nv_bfloat16*>(MODE == kAddrScoresOnly || r < 64 ? A.q0 : A.q1);
       v = __ldg(reinterpret_cast<const uint4*>(q + (size_t)(th * 2 + p) * dh) + c);
     }
     *reinterpret_cast<uint4*>(sA + p * ahalf + tc::kmajor_off(r, 8 * c, dh)) = v;
   }
   for (int e = tid; e < 2 * spad * kc; e += kTcThreads) {
     const int p = e / (spad * kc), rem = e - p * spad * kc;
-    const int j = rem / kc, c = rem - j * kc;
+    const int j = rem >> lkc, c = rem & (kc - 1);
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (j < d.s) {
       const __nv_bfloat16* K = reinterpret_cast<const __nv_bfloat16*>(A.K);
@@ -460,19 +480,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
     // Warps 0-3: half 0, warps 4-7: half 1; lane = row.
     const int g = warp & 3, p = (warp >> 2) & 1;
     const int r = 32 * g + lane;
-    int sg;
-    long long item;
-    tc_row_item<MODE>(r, sg, item);
-    long long th = 0;
-    if (item < BT) {
-      const long long b = item / d.T, t = item - b * d.T;
-      th = (b * d.H + h) * d.T + t;
-    }
+    const long long th = rth[r];
     // Warps 8w .. 8w+7 take every (kTcThreads / 256)-th block of 16 columns.
     for (int c0 = 16 * (warp >> 3); c0 < spad; c0 += 16 * (kTcThreads / 256)) {
       float v[16];
       tc::ld16(tmem + ((uint32_t)(32 * g) << 16) + p * cstride + c0, v);
-      if (item < BT)
+      if (th >= 0)
         for (int i = 0; i < 16; ++i)
           if (c0 + i < d.s) A.S[(size_t)(th * 2 + p) * d.s + c0 + i] = v[i];
     }
@@ -496,10 +509,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
       }
       __syncthreads();
       for (int rr = warp; rr < 32; rr += kTcThreads / 32) {
-        int sg;
-        long long item;
-        tc_row_item<MODE>(32 * g + rr, sg, item);
-        if (item >= BT) continue;
+        const long long th = rth[32 * g + rr];
+        if (th < 0) continue;
+        const int sg = g >> 1;                   // rows 0-63 write, 64-127 read
         const int k = sg == 0 ? d.kw : d.kr;
         const int nsel = sg == 0 ? d.W : d.R;
         float* ov = lv + rr * 2 * kMaxSel;
@@ -515,9 +527,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
           __syncwarp();
         }
         warp_merge(ov, oi, ov + kMaxSel, oi + kMaxSel, k, nsel, (uint32_t)d.s,
-                   stair + sg * kStairMax, nst[sg], ws, lane);
-        const long long b = item / d.T, t = item - b * d.T;
-        const long long th = (b * d.H + h) * d.T + t;
+                   stair + sg * kStairMax, nst[sg], ws, lane, cut + sg * kMaxSel);
         int32_t* io = (sg == 0 ? A.idx_w : A.idx_r) + (size_t)th * nsel;
         float* wo = (sg == 0 ? A.wt_w : A.wt_r) + (size_t)th * nsel;
         warp_softmax_store(ws, nsel, io, wo, lane);

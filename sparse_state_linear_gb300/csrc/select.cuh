@@ -282,7 +282,8 @@ __device__ bool warp_topk_bucketed(const Src& src, int n, int k, WarpScratch& ws
   }
   const float range = vmax - vmin;
   if (!(range > 0.f) || !(range < INFINITY)) return false;
-  const float scale = 256.f / range;
+  // Any positive scale keeps the map monotone (ranks are exact comparisons).
+  const float scale = __fdividef(256.f, range);
   auto bucket = [&](float x) -> uint32_t {
     const float dd = (vmax - x) * scale;
     return min(255u, __float2uint_rz(dd));
@@ -447,16 +448,18 @@ __device__ __forceinline__ int build_stair(int nsel, int k, uint16_t* pairs, int
 }
 
 // Best nsel slots of the two sorted half lists, best first, into ws.out_*.
+// `bcut` (optional) holds nsel / (a + 1) for a < k.
 __device__ __forceinline__ void warp_merge(const float* v1, const uint32_t* id1,
                                            const float* v2, const uint32_t* id2, int k,
                                            int nsel, uint32_t s, const uint16_t* stair,
-                                           int nstair, WarpScratch& ws, int lane) {
+                                           int nstair, WarpScratch& ws, int lane,
+                                           const int* bcut = nullptr) {
   PairSrc ps{v1, id1, v2, id2, stair, s};
   warp_topk<10>(ps, nstair, nsel, ws, lane);
   const float cw = ws.out_v[nsel - 1];
   bool tie = false;
   for (int a = lane; a < k; a += 32) {
-    const int b = nsel / (a + 1);
+    const int b = bcut ? bcut[a] : nsel / (a + 1);
     if (b < k && __fadd_rn(v1[a], v2[b]) >= cw) tie = true;
   }
   if (__any_sync(kFull, tie)) {
@@ -552,7 +555,8 @@ __device__ bool group_topk_bucketed(const Src& src, int n, int k, GroupScratch& 
   }
   const float range = vmax - vmin;
   if (!(range > 0.f) || !(range < INFINITY)) return false;
-  const float scale = 256.f / range;
+  // Any positive scale keeps the map monotone (ranks are exact comparisons).
+  const float scale = __fdividef(256.f, range);
   auto bucket = [&](float x) -> uint32_t {
     const float dd = (vmax - x) * scale;
     return min(255u, __float2uint_rz(dd));

@@ -355,6 +355,11 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
   constexpr int CH = CW / 4;               // 16-byte chunks per row slice
   constexpr int RP = kConsumers / CH;      // rows per consumer pass
   constexpr int IB = BF16 ? 2 : 4;         // input element bytes
+  // Fig. 2 form on 32-float slices: consumer warp c owns column chunk c of
+  // every row (lanes = rows), so the shared prediction and the read are warp
+  // reductions; tile row k keeps its chunk c at 16-byte position c ^ (k & 7)
+  // (conflict-free when the lanes of a warp walk the rows of one chunk).
+  constexpr bool COL = FIG2 && CW == 32;
   extern __shared__ __align__(16) unsigned char smem[];
 
   const Dims& d = A.d;
@@ -529,7 +534,12 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
         const int k = lr + i * LRP;
         if (code[i] != -1) continue;
         const uint32_t off = k < W ? wb + k * rowb : rb + (k - W) * rowb;
-        cp_async16(sm_l + off, Ml + (size_t)row[i] * dv);
+        if constexpr (COL) {
+          const int kk = k < W ? k : k - W;
+          cp_async16(smem + off + 16 * (lc ^ (kk & 7)), Ml + (size_t)row[i] * dv);
+        } else {
+          cp_async16(sm_l + off, Ml + (size_t)row[i] * dv);
+        }
       }
       cp_async_mbar_arrive_noinc(&rfull[rf.i]);
       mu.next();
@@ -542,6 +552,148 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
   }
 
   // -------------------------------------------------------------- consumers
+  if constexpr (COL) {
+    // Warp cc: column chunk cc of every row; lane l: rows l and l + 32 of
+    // the write and read sets.  A step: decay the write rows and reduce the
+    // shared prediction over the lanes, write the rows' new values into the
+    // tile, ONE block barrier, store the step's rows to HBM from the tile
+    // (coalesced, 128 bytes per 8 lanes), weighted read reduced over the
+    // lanes, y chunk stored by lane 0.
+    const int cc = warp;
+    unsigned char* tiles = smem + L.wtile;
+    auto tile_chunk = [&](int slot, int k, int c) -> unsigned char* {
+      return tiles + slot * wslot + k * rowb + 16 * (c ^ (k & 7));
+    };
+    bool aborted = false;
+    Ring mt{0, MR, 0u}, wt{0, NS, 0u}, rf{0, D, 0u};
+    for (int t = 0; t < T; ++t) {
+      if (!aborted) {
+        bool ok = true;
+        if (lane == 0)
+          ok = mbar_wait_bounded(&rfull[rf.i], rf.phase, kTimeoutNs) &&
+               mbar_wait_bounded(&mfull[mt.i], mt.phase, kTimeoutNs);
+        __syncwarp();
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);
+          aborted = true;
+        }
+      }
+      const MetaSlot* m = meta + mt.i;
+      if (!aborted) {
+        const float a = m->alpha, b = m->beta;
+        const float4 vv = load_v4<BF16>(m->vraw, cc);
+        int code[2];
+        float wj[2];
+        float4 md[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int j = lane + 32 * i;
+          code[i] = -2;
+          if (j < W) {
+            code[i] = m->code[j];
+            wj[i] = m->wt_w[j];
+            md[i] = *reinterpret_cast<const float4*>(tile_chunk(wt.i, j, cc));   // fetched copy
+          }
+        }
+        float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int j = lane + 32 * i;
+          if (code[i] == -2) continue;
+          if (code[i] >= 0) {
+            const int dd = code[i] >> 6, p = code[i] & 63;
+            const int sl = wt.i >= dd ? wt.i - dd : wt.i - dd + NS;
+            md[i] = *reinterpret_cast<const float4*>(tile_chunk(sl, p, cc));
+          }
+          if (A.undo)
+            *reinterpret_cast<float4*>(A.undo + ((th0 + t) * W + j) * dv + c0 + 4 * cc) = md[i];
+          md[i] = make_float4(a * md[i].x, a * md[i].y, a * md[i].z, a * md[i].w);
+          part.x = fmaf(wj[i], md[i].x, part.x);
+          part.y = fmaf(wj[i], md[i].y, part.y);
+          part.z = fmaf(wj[i], md[i].z, part.z);
+          part.w = fmaf(wj[i], md[i].w, part.w);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          part.x += __shfl_xor_sync(0xffffffffu, part.x, off);
+          part.y += __shfl_xor_sync(0xffffffffu, part.y, off);
+          part.z += __shfl_xor_sync(0xffffffffu, part.z, off);
+          part.w += __shfl_xor_sync(0xffffffffu, part.w, off);
+        }
+        const float4 res = make_float4(vv.x - part.x, vv.y - part.y, vv.z - part.z, vv.w - part.w);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (code[i] == -2) continue;
+          const float cw = b * wj[i];
+          float4 o;
+          o.x = fmaf(cw, res.x, md[i].x);
+          o.y = fmaf(cw, res.y, md[i].y);
+          o.z = fmaf(cw, res.z, md[i].z);
+          o.w = fmaf(cw, res.w, md[i].w);
+          *reinterpret_cast<float4*>(tile_chunk(wt.i, lane + 32 * i, cc)) = o;
+        }
+      }
+      // The one block barrier of a step (a timeout becomes a uniform exit).
+      if (named_bar_or(1, kConsumers, aborted)) {
+        aborted = true;
+        break;
+      }
+      // The step's rows to HBM from the tile: thread -> (row, chunk).
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int j = (tid >> 3) + 32 * i, c = tid & 7;
+        if (j < W && m->code[j] != -2)
+          *reinterpret_cast<float4*>(Mc + (size_t)m->idx_w[j] * dv + 4 * c) =
+              *reinterpret_cast<const float4*>(tile_chunk(wt.i, j, c));
+      }
+      // Read after the write (Eq. (5)), reduced over the lanes.
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      {
+        int code[2];
+        float w[2];
+        float4 x[2];
+        const unsigned char* rsrc = smem + L.rtile + rf.i * rslot;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int q = lane + 32 * i;
+          code[i] = -2;
+          if (q < R) {
+            code[i] = m->code[W + q];
+            w[i] = m->wt_r[q];
+            x[i] = *reinterpret_cast<const float4*>(rsrc + q * rowb + 16 * (cc ^ (q & 7)));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (code[i] == -2) continue;
+          if (code[i] >= 0) {
+            const int dd = code[i] >> 6, p = code[i] & 63;
+            const int sl = wt.i >= dd ? wt.i - dd : wt.i - dd + NS;
+            x[i] = *reinterpret_cast<const float4*>(tile_chunk(sl, p, cc));
+          }
+          acc.x = fmaf(w[i], x[i].x, acc.x);
+          acc.y = fmaf(w[i], x[i].y, acc.y);
+          acc.z = fmaf(w[i], x[i].z, acc.z);
+          acc.w = fmaf(w[i], x[i].w, acc.w);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+      }
+      if (lane == 0) *reinterpret_cast<float4*>(A.y + (th0 + t) * dv + c0 + 4 * cc) = acc;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mempty[mt.i]);
+      mt.next();
+      wt.next();
+      rf.next();
+    }
+    return;
+  }
+
   const int myc = tid % CH, myr = tid / CH;
   constexpr int kMaxPW = (64 + RP - 1) / RP;   // write / read rows per thread (W, R <= 64)
   constexpr int kMaxPR = kMaxPW;

@@ -270,6 +270,33 @@ def test_scan_matches_oracle(B, H, T, s, dv, W, R, bf16, depth, cs):
             assert np.array_equal(Mg[b, h, untouched], M0[b, h, untouched])
 
 
+@pytest.mark.parametrize("form", [0, 1])
+@pytest.mark.parametrize("depth", [2, 4, 16])
+def test_scan_large_table_reused_rows(form, depth):
+    """More than 65536 rows (the plan's filters then hash rows instead of
+    indexing them) and every step's rows drawn from a pool of 64, so nearly
+    every row is also in flight from the few steps before: the results hinge
+    on the forwarded copies."""
+    B, H, T, s, dv, W, R = 1, 2, 120, 300, 32, 16, 16
+    rng = np.random.default_rng(90000 + depth + 7 * form)
+    N = s * s
+    pool = np.sort(rng.choice(N, 64, replace=False))
+    assert pool.max() >= 65536
+    case = list(random_scan_case(rng, B, H, T, 8, dv, W, R, False))
+    case[0] = np.stack([pool[rng.choice(64, W, replace=False)] for _ in range(B * H * T)])
+    case[0] = case[0].reshape(B, H, T, W).astype(np.int32)
+    case[2] = pool[rng.integers(0, 64, (B, H, T, R))].astype(np.int32)
+    case[-1] = (rng.standard_normal((B, H, N, dv)) * 0.02).astype(np.float32)
+    sh_g = sdm.make_shape(B, H, T, s, 16, dv, W, R, in_dtype=sdm.SDM_F32, update=form)
+    Mg, yg = run_scan(sh_g, case, depth, 16)
+    Mo, yo = oracle_scan(B, H, T, s, dv, W, R, case, update_form=form)
+    assert max_rel(yg, yo) <= FTOL
+    assert max_rel(Mg[:, :, pool], Mo[:, :, pool]) <= FTOL
+    untouched = np.ones(N, bool)
+    untouched[pool] = False
+    assert np.array_equal(Mg[:, :, untouched], case[-1][:, :, untouched])
+
+
 @pytest.mark.parametrize("B,H,T,s,dv,W,R,bf16", [
     (1, 1, 200, 8, 32, 16, 16, False),     # consecutive steps collide constantly
     (2, 3, 150, 16, 64, 32, 48, True),

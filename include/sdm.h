@@ -218,9 +218,11 @@ typedef struct {
  * shapes of 2.8: sqrt N = 240 / 480, d_v = 960 / 1920].  Same arguments and
  * results as sdm_forward (y, M in place, selections in idx_w/wt_w/idx_r/wt_r)
  * plus, when `epi` is non-NULL, the sdm_rmsnorm_gate epilogue on y written
- * to epi->out.  One CTA per (b,h) chain runs that chain's T steps in order,
- * so the latency of a step is one chain's dependent path; use sdm_forward
- * for long T.  Needs no workspace.  Sub-scores are fp32 FFMA for both
+ * to epi->out.  Each (b,h) chain runs its T steps in order on one CTA, or,
+ * when there are too few chains to fill the GPU, on up to 8 CTAs that each
+ * own a range of its columns (with the epilogue they form one thread-block
+ * cluster for the row norm); the latency of a step is one chain's dependent
+ * path; use sdm_forward for long T.  Needs no workspace.  Sub-scores are fp32 FFMA for both
  * input dtypes, so a selection can differ from one made on sdm_forward's
  * tensor-core scores only where two candidate sums are within fp32 rounding
  * of each other. */

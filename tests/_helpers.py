@@ -66,3 +66,26 @@ def max_rel(a: np.ndarray, ref: np.ndarray) -> float:
     if rms == 0.0:
         return float(np.max(np.abs(a - ref))) if a.size else 0.0
     return float(np.max(np.abs(a.astype(np.float64) - ref))) / rms if a.size else 0.0
+
+
+def compact_oracle_scan(idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0_dev, update_form):
+    """The oracle scan of a short segment on a compact table that holds only
+    the rows the segment touches (exact: no other row is ever read)."""
+    B, H, T, W = idx_w.shape
+    R = idx_r.shape[-1]
+    dv = M0_dev.shape[-1]
+    rows = [[np.unique(np.concatenate([idx_w[b, h].ravel(), idx_r[b, h].ravel()]))
+             for h in range(H)] for b in range(B)]
+    n = max(len(r) for rr in rows for r in rr)
+    s2 = int(np.ceil(np.sqrt(n)))
+    Mc = np.zeros((B, H, s2 * s2, dv), np.float32)
+    iw, ir = np.empty_like(idx_w), np.empty_like(idx_r)
+    for b in range(B):
+        for h in range(H):
+            r = rows[b][h]
+            Mc[b, h, :len(r)] = M0_dev[b, h, torch.from_numpy(r).long().to(M0_dev.device)].cpu().numpy()
+            iw[b, h] = np.searchsorted(r, idx_w[b, h])
+            ir[b, h] = np.searchsorted(r, idx_r[b, h])
+    sh = O.Shape(B=B, H=H, T=T, n_sub=s2, d_h=16, d_v=dv, W=W, R=R, update_form=update_form)
+    Mo, yo = O.scan(sh, iw, wt_w, ir, wt_r, alpha, beta, v, Mc)
+    return rows, Mo, yo

@@ -12,7 +12,8 @@ import pytest
 import torch
 
 import oracle as O
-from tests._helpers import FTOL, check_indices, gshape, max_rel, np32, oshape
+from tests._helpers import (FTOL, check_indices, compact_oracle_scan, gshape, max_rel, np32,
+                           oshape)
 from workloads import ORDER, WORKLOADS, generate
 
 pytestmark = pytest.mark.gpu
@@ -89,3 +90,55 @@ def test_fullsize_forward_sampled(name):
             assert torch.equal(Mg[b, h][~touched], M0bh[~touched])
     del g, M, out
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,epi", [("decode_l08", False), ("decode_l13", True)])
+def test_fullsize_decode_sampled(name, epi):
+    """The decode workloads at full size, in the launch configuration the
+    benchmark times (the 8B head shape splits each chain over column parts,
+    a thread-block cluster with the epilogue): every chain's selection
+    against the oracle, and the write, read and epilogue of every chain on
+    the device's selections (the oracle runs on a compact table of the rows
+    a chain touches, copied from M_0 before the call)."""
+    w = WORKLOADS[name]
+    x = generate(w, device=DEV)                 # tables of tens of GB: drawn on the device
+    M = x["M0"]
+    M0 = M.clone()
+    sh = gshape(w, sdm)
+    gate = gamma = None
+    if epi:
+        gen = torch.Generator(device=DEV).manual_seed(11)
+        gate = torch.sigmoid(torch.randn(w.B, w.H, w.T, w.d_v, generator=gen,
+                                         device=DEV)).bfloat16()
+        gamma = torch.rand(w.H, w.d_v, generator=gen, device=DEV) + 0.5
+    out = sdm.sdm_decode(sh, x["q_w"], x["q_r"], x["K"], x["alpha"], x["beta"], x["v"], M,
+                         gate=gate, gamma=gamma, out_dtype=sdm.SDM_F32)
+    assert sdm.sdm_get_device_status() == 0
+    sh_o = oshape(w)
+    S_w = O.subscores(sh_o, np32(x["q_w"]), np32(x["K"]))
+    S_r = O.subscores(sh_o, np32(x["q_r"]), np32(x["K"]))
+    ow, orr = O.select(sh_o, 0, S_w), O.select(sh_o, 1, S_r)
+    iw, ir = out["idx_w"].cpu().numpy(), out["idx_r"].cpu().numpy()
+    check_indices(iw, ow[0], S_w, w.n_sub)
+    check_indices(ir, orr[0], S_r, w.n_sub)
+    ww, wr = np32(out["wt_w"]).astype(np.float64), np32(out["wt_r"]).astype(np.float64)
+    same = np.all(iw == ow[0], axis=-1) & np.all(ir == orr[0], axis=-1)
+    assert same.mean() > 0.9
+    assert np.max(np.abs(ww[same] - ow[2][same]), initial=0) < 1e-5
+    rows, Mo, yo = compact_oracle_scan(iw, ww, ir, wr, np32(x["alpha"]), np32(x["beta"]),
+                                       np32(x["v"]), M0, w.update_form)
+    assert max_rel(np32(out["y"]), yo) <= FTOL
+    for b in range(w.B):
+        for h in range(w.H):
+            r = torch.from_numpy(rows[b][h]).long().to(DEV)
+            assert max_rel(M[b, h, r].cpu().numpy(), Mo[b, h, :len(r)]) <= FTOL
+    if epi:
+        ref = O.rmsnorm_gate(sh_o, yo, np32(gate), np32(gamma), eps=1e-6)
+        assert max_rel(np32(out["out"]), ref) <= FTOL
+    # Rows outside every selection are untouched: compare a random sample.
+    rng = np.random.default_rng(5)
+    for b, h in [(0, 0), (w.B - 1, w.H - 1)]:
+        pick = rng.choice(w.N, 4096, replace=False)
+        pick = np.setdiff1d(pick, iw[b, h].ravel())
+        idx = torch.from_numpy(pick).long().to(DEV)
+        assert torch.equal(M[b, h, idx], M0[b, h, idx])

@@ -8,8 +8,10 @@
 // The Fig. 2 reading of the write ([SDM notes] 2.5) is the second update
 // form: the decayed rows' weighted sum vhat = sum_j w_j M~[j] is one
 // prediction shared by the write set, M[i] = M~[i] + beta_t w_i (v_t - vhat).
-// It needs the whole write set before any row is written: one more block
-// reduction per step.
+// It needs the whole write set before any row is written: on 32-float
+// slices the consumers then own column chunks of every row (a warp
+// reduction, see COL below), on other widths one more block reduction per
+// step.
 //
 // With an undo log ([SDM notes] 2.9, appendix A.3: the backward pass
 // restores earlier states by undoing the in-place sparse writes), the scan
@@ -28,8 +30,9 @@
 //    that step t-d left at write position p (latest such d; reads also see
 //    d = 0, the step's own write), -2 = invalid (index out of range, or a
 //    slot repeated within one write set).  One CTA hashes the write sets of
-//    a block of steps plus the depth-1 steps before it into shared memory
-//    and answers every lookup of the block in parallel.
+//    a block of steps plus the depth-1 steps before it into shared memory;
+//    two filters ("written once", "written again") answer nearly every
+//    lookup at once, and the rest are resolved on the table.
 //  * scan_kernel, one CTA per unit: 8 consumer warps, 1 producer warp and 4
 //    loader warps.  The producer copies each step's slot lists, weights,
 //    codes and value slice into a ring of metadata slots (cp.async, several

@@ -131,6 +131,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
   }
 }
 
+// Bounded wait on two mbarrier phases.  Both are first tested back to back,
+// so in the common case (both complete) their latencies overlap.
+__device__ __forceinline__ bool mbar_wait2_bounded(uint64_t* a, unsigned pa, uint64_t* b,
+                                                   unsigned pb, uint64_t timeout_ns) {
+  const bool ra = mbar_test_wait(a, pa);
+  const bool rb = mbar_test_wait(b, pb);
+  if (ra && rb) return true;
+  return (ra || mbar_wait_bounded(a, pa, timeout_ns)) && (rb || mbar_wait_bounded(b, pb, timeout_ns));
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");

@@ -504,10 +504,10 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
     Ring mu{0, MR, 0u}, me{0, MR, 0u}, rf{0, D, 0u}, lw{0, NS, 0u};
     bool ok = true;
     for (int u = 0; u < T && ok; ++u) {
-      if (lane == 0) {
-        ok = mbar_wait_bounded(&mfull[mu.i], mu.phase, kTimeoutNs);
-        if (ok && u >= D) ok = mbar_wait_bounded(&mempty[me.i], me.phase, kTimeoutNs);
-      }
+      if (lane == 0)
+        ok = u >= D ? mbar_wait2_bounded(&mfull[mu.i], mu.phase, &mempty[me.i], me.phase,
+                                         kTimeoutNs)
+                    : mbar_wait_bounded(&mfull[mu.i], mu.phase, kTimeoutNs);
       __syncwarp();
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
@@ -573,8 +573,7 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
       if (!aborted) {
         bool ok = true;
         if (lane == 0)
-          ok = mbar_wait_bounded(&rfull[rf.i], rf.phase, kTimeoutNs) &&
-               mbar_wait_bounded(&mfull[mt.i], mt.phase, kTimeoutNs);
+          ok = mbar_wait2_bounded(&rfull[rf.i], rf.phase, &mfull[mt.i], mt.phase, kTimeoutNs);
         __syncwarp();
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);
@@ -737,8 +736,7 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
       // Rows of step t landed (and its metadata is decoded).
       bool ok = true;
       if (lane == 0)
-        ok = mbar_wait_bounded(&rfull[rf.i], rf.phase, kTimeoutNs) &&
-             mbar_wait_bounded(&mfull[mt.i], mt.phase, kTimeoutNs);
+        ok = mbar_wait2_bounded(&rfull[rf.i], rf.phase, &mfull[mt.i], mt.phase, kTimeoutNs);
       __syncwarp();
       if (!__shfl_sync(0xffffffffu, ok, 0)) {
         if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);

@@ -731,14 +731,36 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
   Ring wt{0, NS, 0u};   // write-tile slot of step t
   Ring rf{0, D, 0u};    // rows-landed barrier of step t
 
+  // The read sum of step t is reduced over the lanes and stored to the
+  // partials at the top of step t + 1, while that step's barrier tests are
+  // in flight (the partials are read only after step t + 1's block barrier).
+  float4 acc_prev = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto store_partial = [&](int tp, float4 acc) {
+#pragma unroll
+    for (int off = CH; off < 32; off <<= 1) {
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+    }
+    if (lane < CH)
+      *reinterpret_cast<float4*>(ypart + (tp & 1) * 8 * CW + warp * CW + 4 * lane) = acc;
+  };
+
   for (int t = 0; t < T; ++t) {
+    // Rows of step t landed (and its metadata is decoded): every lane tests
+    // both barriers; the previous step's read sum is reduced meanwhile.
+    bool ok = true;
     if (!aborted) {
-      // Rows of step t landed (and its metadata is decoded).
-      bool ok = true;
-      if (lane == 0)
-        ok = mbar_wait2_bounded(&rfull[rf.i], rf.phase, &mfull[mt.i], mt.phase, kTimeoutNs);
-      __syncwarp();
-      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+      const bool r0 = mbar_test_wait(&rfull[rf.i], rf.phase);
+      const bool m0 = mbar_test_wait(&mfull[mt.i], mt.phase);
+      if (t > 0) store_partial(t - 1, acc_prev);
+      if (!__all_sync(0xffffffffu, r0 && m0)) {
+        if (lane == 0)
+          ok = mbar_wait2_bounded(&rfull[rf.i], rf.phase, &mfull[mt.i], mt.phase, kTimeoutNs);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      if (!ok) {
         if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);
         aborted = true;
       }
@@ -886,20 +908,14 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
         acc.w = fmaf(w[pr], x[pr].w, acc.w);
       }
     }
-#pragma unroll
-    for (int off = CH; off < 32; off <<= 1) {
-      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
-      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
-      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
-      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
-    }
-    if (lane < CH) *reinterpret_cast<float4*>(ypart + (t & 1) * 8 * CW + warp * CW + 4 * lane) = acc;
+    acc_prev = acc;
     __syncwarp();
     if (lane == 0) mbar_arrive(&mempty[mt.i]);
     mt.next();
     wt.next();
     rf.next();
   }
+  if (T > 0) store_partial(T - 1, acc_prev);
   named_bar_sync(1, kConsumers);
   if (!aborted && T > 0 && warp == ((T - 1) & 7)) finalize(T - 1);
 }

@@ -161,3 +161,31 @@ def test_python_binding_checks_tensors():
     sh = good_shape()
     with pytest.raises(ValueError):
         sdm.sdm_scan(sh, *([torch.zeros(4)] * 8))
+
+
+def test_decode_arguments(L):
+    sh = good_shape(T=1)
+    dec = lambda ptrs, epi=None, shape=sh: L.sdm_decode(ctypes.byref(shape), *ptrs,
+                                                         ctypes.byref(epi) if epi else None,
+                                                         None)
+    # The twelve tensors must be present and 16-byte aligned.
+    for i in range(12):
+        p = [FAKE] * 12
+        p[i] = None
+        assert dec(p) == 1
+        p[i] = MISALIGNED
+        assert dec(p) == 1
+    # Epilogue: eps > 0 and finite, a known output dtype, gate and output
+    # present, gamma (optional) aligned.
+    good = dict(g=FAKE.value, gamma=None, eps=1e-6, out=FAKE.value, out_dtype=sdm.SDM_F32)
+    for bad in (dict(eps=0.0), dict(eps=float("inf")), dict(eps=float("nan")), dict(out_dtype=7),
+                dict(g=None), dict(out=None), dict(gamma=MISALIGNED.value),
+                dict(out=MISALIGNED.value)):
+        e = sdm.Epilogue(**{**good, **bad})
+        assert dec([FAKE] * 12, e) == 1, bad
+    # Bad shapes are rejected before anything else.
+    assert dec([FAKE] * 12, shape=good_shape(T=1, d_v=2064)) == 2
+    assert dec([FAKE] * 12, shape=good_shape(T=1, W=0)) == 1
+    # No work: returns before looking at the pointers (NULL is fine).
+    for kw in (dict(T=0), dict(B=0), dict(H=0)):
+        assert dec([None] * 12, shape=good_shape(**kw)) == 0

@@ -168,16 +168,19 @@ def job_tokens_per_s(tokens_per_rank_step: int, world: int, steps: int, ms: floa
     return tokens_per_rank_step * world * steps / (ms / 1e3)
 
 
-def traffic_for(kernel_src: str):
-    """DRAM bytes per scan launch recorded by an ncu capture of this exact
-    kernel source (profiles/traffic.json keyed by the source's sha256);
-    None if the kernel changed since."""
+def traffic_for(kernel_srcs):
+    """DRAM bytes per sdm_scan call recorded by an ncu capture of these exact
+    kernel sources (profiles/traffic.json keyed by the sha256 of the files'
+    concatenated bytes); None if a kernel changed since."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
-        with open(kernel_src, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()
+        hs = hashlib.sha256()
+        for src in kernel_srcs:
+            with open(src, "rb") as f:
+                hs.update(f.read())
+        h = hs.hexdigest()
         ent = rec.get(h)
         return None if ent is None else float(ent["bytes_per_launch"])
     except Exception:
@@ -499,7 +502,8 @@ def run_ours(args, w):
                  args.variant, "sdm_scan (plan + scan kernels)")
     traffic = None
     if args.variant in ("forward", "fig2") and w.name == "gdn_matched" and w.update_form == 0:
-        traffic = traffic_for(os.path.join(ROOT, "sparse_state_linear_gb300", "csrc", "scan.cu"))
+        csrc = os.path.join(ROOT, "sparse_state_linear_gb300", "csrc")
+        traffic = traffic_for([os.path.join(csrc, "plan.cu"), os.path.join(csrc, "scan.cu")])
     launches = {"decode": 1, "logged": 3}.get(args.variant, 3)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,

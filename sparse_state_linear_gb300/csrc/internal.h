@@ -33,6 +33,17 @@ cudaError_t launch_address(int mode, const Dims& d, const void* q0, const void* 
                            int32_t* idx_w, float* wt_w, int32_t* idx_r, float* wt_r,
                            float* S, unsigned* status, cudaStream_t stream);
 
+// Plan codes per token: W + R rounded up to 8 (16-byte rows).
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline int code_pitch(int W, int R) { return (W + R + 7) & ~7; }
+
+// Hazard plan (plan.cu): per-row source codes of a segment into `codes`
+// ([B*H*T, code_pitch(W, R)] int16) for a scan of ring depth `depth`.
+cudaError_t launch_plan(const Dims& d, const int32_t* idx_w, const int32_t* idx_r,
+                        int16_t* codes, int depth, unsigned* status, cudaStream_t stream);
+
 // Scan (scan.cu): the plan kernel (writes per-row source codes into
 // `workspace`) then the scan kernel.
 size_t scan_workspace_bytes(const Dims& d);
@@ -43,7 +54,7 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
                         void* workspace, int depth, int col_slice, unsigned* status,
                         cudaStream_t stream);
 
-// Undo of a logged segment (scan.cu): `workspace` holds B*H*N marks.
+// Undo of a logged segment (undo.cu): `workspace` holds B*H*N marks.
 size_t undo_workspace_bytes(const Dims& d);
 cudaError_t launch_undo(const Dims& d, const int32_t* idx_w, const float* undo, float* M,
                         void* workspace, unsigned* status, cudaStream_t stream);

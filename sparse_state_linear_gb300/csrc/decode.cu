@@ -16,12 +16,15 @@
 // and run its T steps in order, each step entirely on chip:
 //   scores    FFMA (or inverse distance) of the four half-queries against
 //             the two sub-key tables, into shared memory;
-//   top-k     warps 0-3, one half-row each (select.cuh, exact);
-//   merge     warps 0-1, staircase merge + softmax (select.cuh);
-//   write     every thread owns 16-byte column chunks of the row and walks
-//             the W write rows in register batches, so the row loads of a
-//             batch are in flight together; Fig. 2 form: a first pass sums
-//             the shared prediction, a second writes;
+//   top-k     four groups of four warps, one half-row each, and
+//   merge     two groups of eight warps, one branch each (staircase merge +
+//             softmax): the bucketed exact selection of select.cuh shared by
+//             a group's warps on a named barrier, with the warp paths as the
+//             exact fallback;
+//   write     every thread owns a 16-byte column chunk and a row group and
+//             walks its W write rows in register batches, so the row loads
+//             of a batch are in flight together; Fig. 2 form: a first pass
+//             sums the shared prediction, a second writes;
 //   read      after a block barrier (the CTA's own global writes are then
 //             visible to all its threads) the R read rows, batched the same
 //             way; optionally the RMS-Norm + gate epilogue, whose row sum of

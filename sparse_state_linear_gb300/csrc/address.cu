@@ -359,7 +359,8 @@ __host__ __device__ inline TcLayout tc_layout(int s, int dh) {
 
 inline bool tc_eligible(const Dims& d) {
   return d.in_dtype == SDM_BF16 && d.score == SDM_SCORE_DOT && d.s <= 256 && d.dh <= 64 &&
-         d.dh % 16 == 0 && (d.dh & (d.dh - 1)) == 0 && tc_layout(d.s, d.dh).total <= 232448;
+         d.dh % 16 == 0 && (d.dh & (d.dh - 1)) == 0 &&
+         tc_layout(d.s, d.dh).total <= device_limits().smem_per_cta;
 }
 
 template <int MODE>

@@ -520,11 +520,11 @@ cudaError_t launch_decode(const Dims& d, const void* q_w, const void* q_r, const
   // Column parts per chain: as many as keep one CTA per SM busy (a CTA of
   // 512 threads at up to 128 registers is alone on its SM), each part at
   // least 32 chunks of 16 bytes wide.
-  constexpr int kSMs = 152;
+  const long long sms = device_limits().sms;
   const int nc4 = d.dv / 4;
   int P = 1;
   for (int p = 2; p <= 8; p *= 2)
-    if (chains * p <= kSMs && nc4 % p == 0 && nc4 / p >= 32) P = p;
+    if (chains * p <= sms && nc4 % p == 0 && nc4 / p >= 32) P = p;
   DecArgs A{d, q_w, q_r, K, alpha, beta, v, M, y, idx_w, wt_w, idx_r, wt_r,
             g, gamma, out, eps, out_dtype, P};
   return d.s <= 256 ? launch_pl<8>(A, stream) : launch_pl<16>(A, stream);

@@ -72,6 +72,15 @@ cudaError_t launch_decode(const Dims& d, const void* q_w, const void* q_r, const
                           const void* g, const float* gamma, float eps, void* out,
                           int out_dtype, cudaStream_t stream);
 
+// Limits of the current device, queried once per device (sdm_api.cu): SM
+// count, shared memory per SM, and the opt-in maximum per CTA.
+struct DeviceLimits {
+  int sms;
+  size_t smem_per_sm;
+  size_t smem_per_cta;
+};
+DeviceLimits device_limits();
+
 // Accessors of the API layer (sdm_api.cu) for other entry points.
 sdm_status api_check_shape(const sdm_shape* shape, Dims* d);
 sdm_status api_status_ptr(unsigned** out);

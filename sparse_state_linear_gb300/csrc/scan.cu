@@ -709,9 +709,6 @@ cudaError_t launch_t(const ScanArgs& A, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-constexpr size_t kSmemPerSM = 233472;   // 228 KiB
-constexpr size_t kSmemMaxCTA = 232448;  // 227 KiB
-constexpr int kSMs = 152;
 
 }  // namespace
 
@@ -726,14 +723,17 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
                         cudaStream_t stream) {
   const long long chains = (long long)d.B * d.H;
   if (chains == 0 || d.T == 0) return cudaSuccess;
+  const DeviceLimits lim = device_limits();
+  const long long sms = lim.sms;
   int cw = col_slice;
-  if (cw == 0) cw = (d.dv % 32 == 0 && chains * (d.dv / 32) >= kSMs) ? 32 : 16;
+  if (cw == 0) cw = (d.dv % 32 == 0 && chains * (d.dv / 32) >= sms) ? 32 : 16;
   if (d.dv % cw != 0) cw = 16;
   const long long units = chains * (d.dv / cw);
   // CTAs per SM needed to keep every unit resident, and the ring depth that fits.
-  const long long per_sm = (units + kSMs - 1) / kSMs;
-  const size_t budget =
-      per_sm <= 1 ? kSmemMaxCTA : (per_sm == 2 ? kSmemPerSM / 2 - 1024 : kSmemPerSM / 3 - 1024);
+  const long long per_sm = (units + sms - 1) / sms;
+  const size_t budget = per_sm <= 1    ? lim.smem_per_cta
+                        : per_sm == 2 ? lim.smem_per_sm / 2 - 1024
+                                      : lim.smem_per_sm / 3 - 1024;
   int D = depth;
   if (D == 0) {
     D = 1;
@@ -742,7 +742,7 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   }
   if (D < 1 || D > 16) return cudaErrorInvalidValue;
   // A requested depth is a hint: shrink it until the ring fits on chip.
-  while (D > 1 && scan_layout(cw, d.W, d.R, D).total > kSmemMaxCTA) --D;
+  while (D > 1 && scan_layout(cw, d.W, d.R, D).total > lim.smem_per_cta) --D;
 
   int16_t* codes = static_cast<int16_t*>(workspace);
   cudaError_t e = launch_plan(d, idx_w, idx_r, codes, D, status, stream);

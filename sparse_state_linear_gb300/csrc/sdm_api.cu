@@ -99,6 +99,25 @@ __global__ void wait_timeout_selftest(unsigned* status, unsigned long long timeo
 
 }  // namespace
 
+DeviceLimits device_limits() {
+  static std::mutex mu;
+  static DeviceLimits cache[64];
+  static bool known[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!known[dev]) {
+    int sms = 0, per_sm = 0, per_cta = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&per_cta, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cache[dev] = DeviceLimits{sms > 0 ? sms : 1, (size_t)(per_sm > 0 ? per_sm : 0),
+                              (size_t)(per_cta > 0 ? per_cta : 0)};
+    known[dev] = true;
+  }
+  return cache[dev];
+}
+
 sdm_status api_check_shape(const sdm_shape* shape, Dims* d) { return check_shape(shape, d); }
 sdm_status api_status_ptr(unsigned** out) { return status_ptr(out); }
 void api_scan_tuning(int* depth, int* col_slice) {

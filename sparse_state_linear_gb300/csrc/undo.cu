@@ -11,8 +11,6 @@
 namespace sdm {
 namespace {
 
-constexpr int kSMs = 152;
-
 // A logged segment is undone by putting back, for every row it wrote, the
 // copy logged at that row's earliest write in the segment.  Three passes
 // over the segment's write sets, as stream-ordered launches (no ordering
@@ -82,12 +80,13 @@ cudaError_t launch_undo(const Dims& d, const int32_t* idx_w, const float* undo, 
   if (n == 0) return cudaSuccess;
   UndoArgs U{idx_w, undo, M, static_cast<uint32_t*>(workspace), n, d.T, d.W, d.dv,
              (uint32_t)d.N(), status};
+  const long long sms = device_limits().sms;
   const long long want = (n + kUndoThreads - 1) / kUndoThreads;
-  const unsigned blocks = (unsigned)(want < 8 * kSMs ? want : 8 * kSMs);
+  const unsigned blocks = (unsigned)(want < 8 * sms ? want : 8 * sms);
   undo_mark_kernel<<<blocks, kUndoThreads, 0, stream>>>(U, 0);
   undo_mark_kernel<<<blocks, kUndoThreads, 0, stream>>>(U, 1);
   const long long wantc = (n + kUndoThreads / 32 - 1) / (kUndoThreads / 32);
-  const unsigned cblocks = (unsigned)(wantc < 16 * kSMs ? wantc : 16 * kSMs);
+  const unsigned cblocks = (unsigned)(wantc < 16 * sms ? wantc : 16 * sms);
   undo_copy_kernel<<<cblocks, kUndoThreads, 0, stream>>>(U);
   return cudaGetLastError();
 }

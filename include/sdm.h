@@ -32,6 +32,11 @@
  *  - The library allocates no device memory (the status word is a static
  *    device variable; scratch is the caller's `workspace`).  There is no
  *    CPU fallback.
+ *  - The device addresses of the library's static device arrays (the status
+ *    word; the scratch of sdm_scan_noalloc) are looked up once per device and
+ *    kept for the life of the process: do not go on using the library on a
+ *    device after cudaDeviceReset (or any other teardown of its primary
+ *    context), since those addresses are then stale.
  */
 #ifndef SDM_H
 #define SDM_H

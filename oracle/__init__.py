@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "sdm_oracle.cpp")
 _LIB = os.path.join(_HERE, "_build", "libsdm_oracle.so")
 
-__all__ = ["build", "Shape", "subscores", "select", "scan", "forward"]
+__all__ = ["build", "Shape", "subscores", "select", "slot_weights", "scan", "forward"]
 
 
 def build(force: bool = False) -> str:
@@ -82,12 +82,14 @@ def _L():
         sp = ctypes.POINTER(_CShape)
         _lib.sdm_ref_subscores.argtypes = [sp, P, P, P]
         _lib.sdm_ref_select.argtypes = [sp, ctypes.c_int, P, P, P, P]
+        _lib.sdm_ref_slot_weights.argtypes = [sp, ctypes.c_int, P, P, P]
         _lib.sdm_ref_scan.argtypes = [sp] + [P] * 9
         _lib.sdm_ref_forward.argtypes = [sp] + [P] * 12
         _lib.sdm_ref_scan_logged.argtypes = [sp] + [P] * 10
         _lib.sdm_ref_undo.argtypes = [sp] + [P] * 3
         _lib.sdm_ref_rmsnorm_gate.argtypes = [sp, P, P, P, ctypes.c_double, P]
-        for f in (_lib.sdm_ref_subscores, _lib.sdm_ref_select, _lib.sdm_ref_scan,
+        for f in (_lib.sdm_ref_subscores, _lib.sdm_ref_select, _lib.sdm_ref_slot_weights,
+                  _lib.sdm_ref_scan,
                   _lib.sdm_ref_forward, _lib.sdm_ref_scan_logged, _lib.sdm_ref_undo,
                   _lib.sdm_ref_rmsnorm_gate):
             f.restype = ctypes.c_int
@@ -132,6 +134,22 @@ def select(sh: Shape, which: int, S):
     _check(_L().sdm_ref_select(ctypes.byref(cs), which, _p(S), _p(idx), _p(sc), _p(wt)),
            "select")
     return idx, sc, wt
+
+
+def slot_weights(sh: Shape, which: int, S, idx) -> np.ndarray:
+    """Softmax weights (float64 [B,H,T,n]) of the given slot lists idx
+    [B,H,T,n] from float32 sub-scores S [B,H,T,2,s]: the oracle's weights for
+    a selection made elsewhere."""
+    S = _arr(S, np.float32)
+    idx = _arr(idx, np.int32)
+    n = sh.W if which == 0 else sh.R
+    assert S.shape == (sh.B, sh.H, sh.T, 2, sh.n_sub), S.shape
+    assert idx.shape == (sh.B, sh.H, sh.T, n), idx.shape
+    wt = np.empty(idx.shape, np.float64)
+    cs = sh.c()
+    _check(_L().sdm_ref_slot_weights(ctypes.byref(cs), which, _p(S), _p(idx), _p(wt)),
+           "slot_weights")
+    return wt
 
 
 def scan(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M0, log: bool = False):

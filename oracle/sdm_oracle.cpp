@@ -135,6 +135,40 @@ extern "C" int sdm_ref_select(const sdm_ref_shape* sh, int which, const float* S
   return 0;
 }
 
+// [SDM notes] 2.3 / 2.2 again, for a slot list chosen elsewhere: the weight
+// of each listed slot is the softmax over the listed slots' float sums
+// fl(S1[a] + S2[b]) (slot = a*s + b), max subtracted, sum in list order.
+// Parity tests use it to give the oracle's own weights to a selection the
+// device made, when that selection legitimately differs from the oracle's
+// inside the score-gap tolerance.
+extern "C" int sdm_ref_slot_weights(const sdm_ref_shape* sh, int which, const float* S,
+                                    const int32_t* idx, double* wt) {
+  if (!shape_ok(sh) || !S || !idx || !wt) return -1;
+  if (which != 0 && which != 1) return -1;
+  const int s = sh->n_sub;
+  const int n_sel = which == 0 ? sh->W : sh->R;
+  const long long N = (long long)s * s;
+  std::vector<double> c(n_sel);
+  for (size_t row = 0; row < (size_t)sh->B * sh->H * sh->T; ++row) {
+    const float* s1 = S + (row * 2 + 0) * s;
+    const float* s2 = S + (row * 2 + 1) * s;
+    double mx = -INFINITY;
+    for (int j = 0; j < n_sel; ++j) {
+      const int32_t slot = idx[row * n_sel + j];
+      if (slot < 0 || slot >= N) return -2;
+      c[j] = (double)(float)(s1[slot / s] + s2[slot % s]);
+      if (c[j] > mx) mx = c[j];
+    }
+    double tot = 0.0;
+    for (int j = 0; j < n_sel; ++j) {
+      c[j] = std::exp(c[j] - mx);
+      tot += c[j];
+    }
+    for (int j = 0; j < n_sel; ++j) wt[row * n_sel + j] = c[j] / tot;
+  }
+  return 0;
+}
+
 // [SDM notes] 2.4, Eq. (3)-(4): for i in the write set,
 //   M~[i] = alpha_t M[i];  M[i] = M~[i] + beta_t k^(i) (v_t - M~[i]);
 // rows outside the write set are left exactly as they were (no global decay).

@@ -58,6 +58,13 @@ int sdm_ref_subscores(const sdm_ref_shape* sh, const float* q, const float* K,
 int sdm_ref_select(const sdm_ref_shape* sh, int which, const float* S,
                    int32_t* idx, float* score, double* wt);
 
+/* Softmax weights of a given slot list: idx [B,H,T,n_sel] (n_sel = W for
+ * which = 0, R for which = 1; slots in any order) against float sub-scores
+ * S [B,H,T,2,s]; wt [B,H,T,n_sel] (double) is the softmax of the listed
+ * slots' float sums fl(S1[a] + S2[b]).  Returns -2 for a slot outside [0, N). */
+int sdm_ref_slot_weights(const sdm_ref_shape* sh, int which, const float* S,
+                         const int32_t* idx, double* wt);
+
 /* The write-then-read recurrence, sequential in t, for every (b,h) chain.
  * idx_w/wt_w: [B,H,T,W]; idx_r/wt_r: [B,H,T,R]; alpha, beta: [B,H,T];
  * v: [B,H,T,d_v]; M: [B,H,N,d_v] in/out (double); y: [B,H,T,d_v] out. */

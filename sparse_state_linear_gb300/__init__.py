@@ -2,8 +2,9 @@
 
 Thin ctypes marshalling over ``_build/libsdm_gb300.so`` (the C ABI in
 ``include/sdm.h``): every function here has the name of the C entry point it
-calls, checks that tensors are CUDA, contiguous and of the right dtype, and
-passes device pointers and the current CUDA stream.  All arithmetic runs in
+calls, checks that tensors are CUDA tensors on the current device, contiguous,
+of the right dtype and at least as large as the shape implies, and passes
+device pointers and the current CUDA stream.  All arithmetic runs in
 the library's kernels; there is no CPU fallback.  If the library is not
 built, importing works but every call raises ``SdmUnavailable``.
 """
@@ -124,16 +125,35 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _ptr(t: torch.Tensor | None, name: str, dtypes=None):
+def _ptr(t: torch.Tensor | None, name: str, dtypes=None, numel: int | None = None):
+    """Device pointer of `t` after checking that it is a contiguous CUDA
+    tensor on the current device (the library launches there), of one of
+    `dtypes`, with at least `numel` elements (the size the shape implies)."""
     if t is None:
         raise ValueError(f"{name} is required")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()}; call under "
+                         f"torch.cuda.device({t.device})")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtypes is not None and t.dtype not in dtypes:
         raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, the shape needs {numel}")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _sizes(sh: Shape):
+    """Elements each argument needs for this shape."""
+    bht = sh.B * sh.H * sh.T
+    if bht == 0:               # no work: the library does not look at the pointers
+        return dict.fromkeys(("q", "K", "S", "W", "R", "g", "v", "M", "y", "U", "gamma"), 0)
+    return dict(q=bht * 2 * sh.d_h, K=sh.H * 2 * sh.n_sub * sh.d_h, S=bht * 2 * sh.n_sub,
+                W=bht * sh.W, R=bht * sh.R, g=bht, v=bht * sh.d_v, M=sh.B * sh.H * sh.N * sh.d_v,
+                y=bht * sh.d_v, U=bht * sh.W * sh.d_v, gamma=sh.H * sh.d_v)
 
 
 def _in_dt(sh: Shape):
@@ -153,8 +173,11 @@ def sdm_subscores(sh: Shape, q, K, S=None, stream=None):
     """Sub-scores [B,H,T,2,s] float32 of one branch's half-queries q [B,H,T,2,d_h]."""
     if S is None:
         S = _empty((sh.B, sh.H, sh.T, 2, sh.n_sub), torch.float32, q)
-    _ok(lib().sdm_subscores(ctypes.byref(sh), _ptr(q, "q", _in_dt(sh)), _ptr(K, "K", _in_dt(sh)),
-                            _ptr(S, "S", (torch.float32,)), _stream(stream)), "sdm_subscores")
+    n = _sizes(sh)
+    _ok(lib().sdm_subscores(ctypes.byref(sh), _ptr(q, "q", _in_dt(sh), n["q"]),
+                            _ptr(K, "K", _in_dt(sh), n["K"]),
+                            _ptr(S, "S", (torch.float32,), n["S"]), _stream(stream)),
+        "sdm_subscores")
     return S
 
 
@@ -171,10 +194,12 @@ def sdm_select(sh: Shape, sub_w, sub_r, idx_w=None, wt_w=None, idx_r=None, wt_r=
                stream=None):
     """Product-key selection from float32 sub-scores; returns (idx_w, wt_w, idx_r, wt_r)."""
     idx_w, wt_w, idx_r, wt_r = _sel_outputs(sh, sub_w, idx_w, wt_w, idx_r, wt_r)
-    f32, i32 = (torch.float32,), (torch.int32,)
-    _ok(lib().sdm_select(ctypes.byref(sh), _ptr(sub_w, "sub_w", f32), _ptr(sub_r, "sub_r", f32),
-                         _ptr(idx_w, "idx_w", i32), _ptr(wt_w, "wt_w", f32),
-                         _ptr(idx_r, "idx_r", i32), _ptr(wt_r, "wt_r", f32), _stream(stream)),
+    f32, i32, n = (torch.float32,), (torch.int32,), _sizes(sh)
+    _ok(lib().sdm_select(ctypes.byref(sh), _ptr(sub_w, "sub_w", f32, n["S"]),
+                         _ptr(sub_r, "sub_r", f32, n["S"]),
+                         _ptr(idx_w, "idx_w", i32, n["W"]), _ptr(wt_w, "wt_w", f32, n["W"]),
+                         _ptr(idx_r, "idx_r", i32, n["R"]), _ptr(wt_r, "wt_r", f32, n["R"]),
+                         _stream(stream)),
         "sdm_select")
     return idx_w, wt_w, idx_r, wt_r
 
@@ -183,10 +208,12 @@ def sdm_address(sh: Shape, q_w, q_r, K, idx_w=None, wt_w=None, idx_r=None, wt_r=
                 stream=None):
     """Fused sub-scores + selection; returns (idx_w, wt_w, idx_r, wt_r)."""
     idx_w, wt_w, idx_r, wt_r = _sel_outputs(sh, q_w, idx_w, wt_w, idx_r, wt_r)
-    dt, f32, i32 = _in_dt(sh), (torch.float32,), (torch.int32,)
-    _ok(lib().sdm_address(ctypes.byref(sh), _ptr(q_w, "q_w", dt), _ptr(q_r, "q_r", dt),
-                          _ptr(K, "K", dt), _ptr(idx_w, "idx_w", i32), _ptr(wt_w, "wt_w", f32),
-                          _ptr(idx_r, "idx_r", i32), _ptr(wt_r, "wt_r", f32), _stream(stream)),
+    dt, f32, i32, n = _in_dt(sh), (torch.float32,), (torch.int32,), _sizes(sh)
+    _ok(lib().sdm_address(ctypes.byref(sh), _ptr(q_w, "q_w", dt, n["q"]),
+                          _ptr(q_r, "q_r", dt, n["q"]), _ptr(K, "K", dt, n["K"]),
+                          _ptr(idx_w, "idx_w", i32, n["W"]), _ptr(wt_w, "wt_w", f32, n["W"]),
+                          _ptr(idx_r, "idx_r", i32, n["R"]), _ptr(wt_r, "wt_r", f32, n["R"]),
+                          _stream(stream)),
         "sdm_address")
     return idx_w, wt_w, idx_r, wt_r
 
@@ -210,10 +237,13 @@ def sdm_scan(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y=None, wor
         y = _empty((sh.B, sh.H, sh.T, sh.d_v), torch.float32, M)
     ws, nws = _workspace(sh, M, workspace)
     dt, f32, i32 = _in_dt(sh), (torch.float32,), (torch.int32,)
-    _ok(lib().sdm_scan(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32), _ptr(wt_w, "wt_w", f32),
-                       _ptr(idx_r, "idx_r", i32), _ptr(wt_r, "wt_r", f32),
-                       _ptr(alpha, "alpha", dt), _ptr(beta, "beta", dt), _ptr(v, "v", dt),
-                       _ptr(M, "M", f32), _ptr(y, "y", f32), _ptr(ws, "workspace"), nws,
+    n = _sizes(sh)
+    _ok(lib().sdm_scan(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32, n["W"]),
+                       _ptr(wt_w, "wt_w", f32, n["W"]), _ptr(idx_r, "idx_r", i32, n["R"]),
+                       _ptr(wt_r, "wt_r", f32, n["R"]), _ptr(alpha, "alpha", dt, n["g"]),
+                       _ptr(beta, "beta", dt, n["g"]), _ptr(v, "v", dt, n["v"]),
+                       _ptr(M, "M", f32, n["M"]), _ptr(y, "y", f32, n["y"]),
+                       _ptr(ws, "workspace"), nws,
                        _stream(stream)), "sdm_scan")
     return y
 
@@ -225,11 +255,13 @@ def sdm_scan_noalloc(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y=N
     if y is None:
         y = _empty((sh.B, sh.H, sh.T, sh.d_v), torch.float32, M)
     dt, f32, i32 = _in_dt(sh), (torch.float32,), (torch.int32,)
-    _ok(lib().sdm_scan_noalloc(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32),
-                               _ptr(wt_w, "wt_w", f32), _ptr(idx_r, "idx_r", i32),
-                               _ptr(wt_r, "wt_r", f32), _ptr(alpha, "alpha", dt),
-                               _ptr(beta, "beta", dt), _ptr(v, "v", dt), _ptr(M, "M", f32),
-                               _ptr(y, "y", f32), _stream(stream)), "sdm_scan_noalloc")
+    n = _sizes(sh)
+    _ok(lib().sdm_scan_noalloc(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32, n["W"]),
+                               _ptr(wt_w, "wt_w", f32, n["W"]), _ptr(idx_r, "idx_r", i32, n["R"]),
+                               _ptr(wt_r, "wt_r", f32, n["R"]),
+                               _ptr(alpha, "alpha", dt, n["g"]), _ptr(beta, "beta", dt, n["g"]),
+                               _ptr(v, "v", dt, n["v"]), _ptr(M, "M", f32, n["M"]),
+                               _ptr(y, "y", f32, n["y"]), _stream(stream)), "sdm_scan_noalloc")
     return y
 
 
@@ -243,11 +275,14 @@ def sdm_scan_logged(sh: Shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y=No
         undo = _empty((sh.B, sh.H, sh.T, sh.W, sh.d_v), torch.float32, M)
     ws, nws = _workspace(sh, M, workspace)
     dt, f32, i32 = _in_dt(sh), (torch.float32,), (torch.int32,)
-    _ok(lib().sdm_scan_logged(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32),
-                              _ptr(wt_w, "wt_w", f32), _ptr(idx_r, "idx_r", i32),
-                              _ptr(wt_r, "wt_r", f32), _ptr(alpha, "alpha", dt),
-                              _ptr(beta, "beta", dt), _ptr(v, "v", dt), _ptr(M, "M", f32),
-                              _ptr(y, "y", f32), _ptr(undo, "undo", f32), _ptr(ws, "workspace"),
+    n = _sizes(sh)
+    _ok(lib().sdm_scan_logged(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32, n["W"]),
+                              _ptr(wt_w, "wt_w", f32, n["W"]), _ptr(idx_r, "idx_r", i32, n["R"]),
+                              _ptr(wt_r, "wt_r", f32, n["R"]),
+                              _ptr(alpha, "alpha", dt, n["g"]), _ptr(beta, "beta", dt, n["g"]),
+                              _ptr(v, "v", dt, n["v"]), _ptr(M, "M", f32, n["M"]),
+                              _ptr(y, "y", f32, n["y"]), _ptr(undo, "undo", f32, n["U"]),
+                              _ptr(ws, "workspace"),
                               nws, _stream(stream)), "sdm_scan_logged")
     return y, undo
 
@@ -264,8 +299,9 @@ def sdm_scan_undo(sh: Shape, idx_w, undo, M, workspace=None, stream=None):
                                 device=M.device)
     nws = workspace.numel() * workspace.element_size()
     f32, i32 = (torch.float32,), (torch.int32,)
-    _ok(lib().sdm_scan_undo(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32),
-                            _ptr(undo, "undo", f32), _ptr(M, "M", f32),
+    n = _sizes(sh)
+    _ok(lib().sdm_scan_undo(ctypes.byref(sh), _ptr(idx_w, "idx_w", i32, n["W"]),
+                            _ptr(undo, "undo", f32, n["U"]), _ptr(M, "M", f32, n["M"]),
                             _ptr(workspace, "workspace"), nws, _stream(stream)),
         "sdm_scan_undo")
     return M
@@ -279,9 +315,11 @@ def sdm_rmsnorm_gate(sh: Shape, y, g, gamma=None, eps: float = 1e-6, out=None,
     if out is None:
         out = _empty((sh.B, sh.H, sh.T, sh.d_v), tdt, y)
     f32 = (torch.float32,)
-    gp = None if gamma is None else _ptr(gamma, "gamma", f32)
-    _ok(lib().sdm_rmsnorm_gate(ctypes.byref(sh), _ptr(y, "y", f32), _ptr(g, "g", _in_dt(sh)), gp,
-                               float(eps), _ptr(out, "out", (tdt,)), int(out_dtype),
+    n = _sizes(sh)
+    gp = None if gamma is None else _ptr(gamma, "gamma", f32, n["gamma"])
+    _ok(lib().sdm_rmsnorm_gate(ctypes.byref(sh), _ptr(y, "y", f32, n["y"]),
+                               _ptr(g, "g", _in_dt(sh), n["y"]), gp,
+                               float(eps), _ptr(out, "out", (tdt,), n["y"]), int(out_dtype),
                                _stream(stream)), "sdm_rmsnorm_gate")
     return out
 
@@ -295,20 +333,22 @@ def sdm_decode(sh: Shape, q_w, q_r, K, alpha, beta, v, M, y=None, idx_w=None, wt
     if y is None:
         y = _empty((sh.B, sh.H, sh.T, sh.d_v), torch.float32, M)
     idx_w, wt_w, idx_r, wt_r = _sel_outputs(sh, M, idx_w, wt_w, idx_r, wt_r)
-    dt, f32, i32 = _in_dt(sh), (torch.float32,), (torch.int32,)
+    dt, f32, i32, n = _in_dt(sh), (torch.float32,), (torch.int32,), _sizes(sh)
     epi = None
     if gate is not None:
         tdt = torch.bfloat16 if out_dtype == SDM_BF16 else torch.float32
         if out is None:
             out = _empty((sh.B, sh.H, sh.T, sh.d_v), tdt, M)
-        epi = Epilogue(_ptr(gate, "gate", dt).value,
-                       None if gamma is None else _ptr(gamma, "gamma", f32).value,
-                       float(eps), _ptr(out, "out", (tdt,)).value, int(out_dtype))
-    _ok(lib().sdm_decode(ctypes.byref(sh), _ptr(q_w, "q_w", dt), _ptr(q_r, "q_r", dt),
-                         _ptr(K, "K", dt), _ptr(alpha, "alpha", dt), _ptr(beta, "beta", dt),
-                         _ptr(v, "v", dt), _ptr(M, "M", f32), _ptr(y, "y", f32),
-                         _ptr(idx_w, "idx_w", i32), _ptr(wt_w, "wt_w", f32),
-                         _ptr(idx_r, "idx_r", i32), _ptr(wt_r, "wt_r", f32),
+        epi = Epilogue(_ptr(gate, "gate", dt, n["y"]).value,
+                       None if gamma is None else _ptr(gamma, "gamma", f32, n["gamma"]).value,
+                       float(eps), _ptr(out, "out", (tdt,), n["y"]).value, int(out_dtype))
+    _ok(lib().sdm_decode(ctypes.byref(sh), _ptr(q_w, "q_w", dt, n["q"]),
+                         _ptr(q_r, "q_r", dt, n["q"]), _ptr(K, "K", dt, n["K"]),
+                         _ptr(alpha, "alpha", dt, n["g"]), _ptr(beta, "beta", dt, n["g"]),
+                         _ptr(v, "v", dt, n["v"]), _ptr(M, "M", f32, n["M"]),
+                         _ptr(y, "y", f32, n["y"]),
+                         _ptr(idx_w, "idx_w", i32, n["W"]), _ptr(wt_w, "wt_w", f32, n["W"]),
+                         _ptr(idx_r, "idx_r", i32, n["R"]), _ptr(wt_r, "wt_r", f32, n["R"]),
                          None if epi is None else ctypes.byref(epi), _stream(stream)),
         "sdm_decode")
     return dict(y=y, idx_w=idx_w, wt_w=wt_w, idx_r=idx_r, wt_r=wt_r, out=out)
@@ -322,11 +362,14 @@ def sdm_forward(sh: Shape, q_w, q_r, K, alpha, beta, v, M, y=None, idx_w=None, w
     idx_w, wt_w, idx_r, wt_r = _sel_outputs(sh, M, idx_w, wt_w, idx_r, wt_r)
     ws, nws = _workspace(sh, M, workspace)
     dt, f32, i32 = _in_dt(sh), (torch.float32,), (torch.int32,)
-    _ok(lib().sdm_forward(ctypes.byref(sh), _ptr(q_w, "q_w", dt), _ptr(q_r, "q_r", dt),
-                          _ptr(K, "K", dt), _ptr(alpha, "alpha", dt), _ptr(beta, "beta", dt),
-                          _ptr(v, "v", dt), _ptr(M, "M", f32), _ptr(y, "y", f32),
-                          _ptr(idx_w, "idx_w", i32), _ptr(wt_w, "wt_w", f32),
-                          _ptr(idx_r, "idx_r", i32), _ptr(wt_r, "wt_r", f32),
+    n = _sizes(sh)
+    _ok(lib().sdm_forward(ctypes.byref(sh), _ptr(q_w, "q_w", dt, n["q"]),
+                          _ptr(q_r, "q_r", dt, n["q"]), _ptr(K, "K", dt, n["K"]),
+                          _ptr(alpha, "alpha", dt, n["g"]), _ptr(beta, "beta", dt, n["g"]),
+                          _ptr(v, "v", dt, n["v"]), _ptr(M, "M", f32, n["M"]),
+                          _ptr(y, "y", f32, n["y"]),
+                          _ptr(idx_w, "idx_w", i32, n["W"]), _ptr(wt_w, "wt_w", f32, n["W"]),
+                          _ptr(idx_r, "idx_r", i32, n["R"]), _ptr(wt_r, "wt_r", f32, n["R"]),
                           _ptr(ws, "workspace"), nws, _stream(stream)), "sdm_forward")
     return dict(y=y, idx_w=idx_w, wt_w=wt_w, idx_r=idx_r, wt_r=wt_r)
 

@@ -11,6 +11,9 @@ import oracle as O
 # floats within max-abs 1e-4 x RMS of the oracle's output.
 GAP = 1e-5
 FTOL = 1e-4
+# Device softmax weights (fp32, from the device's sub-scores) against the
+# oracle's (double, from its own sub-scores) for the same slots.
+WTOL = 1e-5
 
 
 def oshape(w, T=None, B=None, H=None):
@@ -59,6 +62,21 @@ def check_indices(idx_gpu, idx_ref, S_ref, n_sub, gap=GAP):
             assert np.all(np.diff(sg) <= gap), f"row {r}: order {sg}"
         bad_rows += 1
     return bad_rows
+
+
+def oracle_weights(sh_o, S_w, S_r, iw, ir, ww=None, wr=None):
+    """The oracle's weights for the device's selections iw / ir: the softmax
+    of the oracle's own float sums (from its sub-scores S_w / S_r) of exactly
+    those slots, in the device's order.  With the device's weights given,
+    asserts they agree within WTOL on every row.  Returns (wt_w, wt_r) float64,
+    the weights a re-anchored oracle scan takes."""
+    ow = O.slot_weights(sh_o, 0, S_w, iw)
+    orr = O.slot_weights(sh_o, 1, S_r, ir)
+    if ww is not None:
+        assert np.max(np.abs(np.asarray(ww, np.float64) - ow), initial=0) < WTOL
+    if wr is not None:
+        assert np.max(np.abs(np.asarray(wr, np.float64) - orr), initial=0) < WTOL
+    return ow, orr
 
 
 def max_rel(a: np.ndarray, ref: np.ndarray) -> float:

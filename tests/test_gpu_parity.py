@@ -9,7 +9,7 @@ import torch
 
 import oracle as O
 from tests._helpers import (FTOL, check_indices, compact_oracle_scan, gshape, max_rel, np32,
-                           oshape)
+                           oracle_weights, oshape)
 from workloads import WORKLOADS, generate
 
 pytestmark = pytest.mark.gpu
@@ -149,8 +149,9 @@ def test_address_end_to_end(name):
     # Differences are allowed only inside the 1e-5 score gap (asserted inside).
     check_indices(iw, ow[0], S_w, w.n_sub)
     check_indices(ir, orr[0], S_r, w.n_sub)
-    same = np.all(iw == ow[0], axis=-1)
-    assert np.max(np.abs(ww[same] - ow[2][same])) < 1e-5
+    # Weights on every row: the oracle's softmax of its own sums for the
+    # device's slots (equal to its selection's weights where the slots agree).
+    oracle_weights(sh_o, S_w, S_r, iw, ir, ww, wr)
 
 
 ROW_SHAPES = [  # bf16 dot scores: the one-thread-per-row kernel
@@ -380,28 +381,32 @@ def test_forward_fig2_end_to_end(name):
 
 
 def forward_check(w):
+    """sdm_forward against the oracle.  Selections: equal to the oracle's, or
+    different only inside the score gap.  Floats: against the oracle scan
+    re-anchored on the device's slots, with weights the oracle computes for
+    those slots from its own sub-scores (device weights checked on every
+    row); where the slots agree this is the oracle's own forward."""
     x = generate(w)
     sh_g, sh_o = gshape(w, sdm), oshape(w)
     g = {k: t.to(DEV) for k, t in x.items()}
     M = g["M0"].clone()
     out = sdm.sdm_forward(sh_g, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M)
     status_ok()
-    ref = O.forward(sh_o, *(np32(x[k]) for k in ("q_w", "q_r", "K", "alpha", "beta", "v")),
-                    x["M0"].numpy())
+    ins = [np32(x[k]) for k in ("q_w", "q_r", "K", "alpha", "beta", "v")]
+    ref = O.forward(sh_o, *ins, x["M0"].numpy())
     iw, ir = out["idx_w"].cpu().numpy(), out["idx_r"].cpu().numpy()
-    if np.array_equal(iw, ref["idx_w"]) and np.array_equal(ir, ref["idx_r"]):
-        yo, Mo = ref["y"], ref["M"]
-    else:
-        # Re-anchor: the oracle scan follows the device's selections.
-        S_w = O.subscores(sh_o, np32(x["q_w"]), np32(x["K"]))
-        S_r = O.subscores(sh_o, np32(x["q_r"]), np32(x["K"]))
-        check_indices(iw, ref["idx_w"], S_w, w.n_sub)
-        check_indices(ir, ref["idx_r"], S_r, w.n_sub)
-        Mo, yo = O.scan(sh_o, iw, np32(out["wt_w"]).astype(np.float64), ir,
-                        np32(out["wt_r"]).astype(np.float64), np32(x["alpha"]),
-                        np32(x["beta"]), np32(x["v"]), x["M0"].numpy())
+    S_w = O.subscores(sh_o, ins[0], ins[2])
+    S_r = O.subscores(sh_o, ins[1], ins[2])
+    check_indices(iw, ref["idx_w"], S_w, w.n_sub)
+    check_indices(ir, ref["idx_r"], S_r, w.n_sub)
+    ow, orr = oracle_weights(sh_o, S_w, S_r, iw, ir, np32(out["wt_w"]), np32(out["wt_r"]))
+    Mo, yo = O.scan(sh_o, iw, ow, ir, orr, ins[3], ins[4], ins[5], x["M0"].numpy())
     assert max_rel(np32(out["y"]), yo) <= FTOL
     assert max_rel(M.cpu().numpy(), Mo) <= FTOL
+    if np.array_equal(iw, ref["idx_w"]) and np.array_equal(ir, ref["idx_r"]):
+        # Same selections: the re-anchored scan is the oracle's own forward.
+        assert np.array_equal(yo, ref["y"]) and np.array_equal(Mo, ref["M"])
+    return out, ref, yo
 
 
 # ------------------------------------------------------------------ edge cases
@@ -413,6 +418,26 @@ def test_empty_inputs_are_no_ops():
     sdm.sdm_scan(sh, zi, z, zi, z, z, z, z, z, y=z)
     sh = sdm.make_shape(1, 1, 0, 8, 16, 32, 4, 4, in_dtype=sdm.SDM_F32)
     sdm.sdm_forward(sh, z, z, z, z, z, z, z, y=z, idx_w=zi, wt_w=z, idx_r=zi, wt_r=z)
+    status_ok()
+
+
+def test_binding_checks_sizes_and_device_before_the_call():
+    """The Python binding refuses a tensor smaller than the shape implies
+    (before anything reaches the library) and a tensor on a device other than
+    the current one."""
+    w = WORKLOADS["tiny"].with_(T=10)
+    x = generate(w)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    sh = gshape(w, sdm)
+    with pytest.raises(ValueError, match="elements"):
+        sdm.sdm_address(sh, g["q_w"][:, :, :5].contiguous(), g["q_r"], g["K"])
+    M_small = g["M0"][:, :, :16].contiguous()
+    sel = sdm.sdm_address(sh, g["q_w"], g["q_r"], g["K"])
+    with pytest.raises(ValueError, match="elements"):
+        sdm.sdm_scan(sh, *sel, g["alpha"], g["beta"], g["v"], M_small)
+    if torch.cuda.device_count() > 1:
+        with pytest.raises(ValueError, match="current device"):
+            sdm.sdm_address(sh, g["q_w"].to("cuda:1"), g["q_r"], g["K"])
     status_ok()
 
 
@@ -559,21 +584,18 @@ def test_rmsnorm_gate_matches_oracle(B, H, T, dv, bf16, out_dtype):
 
 
 def test_forward_then_epilogue_matches_oracle():
+    """sdm_forward then sdm_rmsnorm_gate against the oracle epilogue of the
+    re-anchored oracle read (asserts on every row, whether or not the
+    device's selections equal the oracle's)."""
     w = WORKLOADS["gdn_matched"].with_(B=1, H=2, T=120)
-    x = generate(w)
+    gate = torch.sigmoid(torch.randn(w.B, w.H, w.T, w.d_v,
+                                     generator=torch.Generator().manual_seed(3))).to(torch.bfloat16)
+    out, _, yo = forward_check(w)
     sh_g, sh_o = gshape(w, sdm), oshape(w)
-    g = {k: t.to(DEV) for k, t in x.items()}
-    gate = torch.sigmoid(torch.randn(w.B, w.H, w.T, w.d_v, generator=torch.Generator().manual_seed(3))).to(torch.bfloat16)
-    M = g["M0"].clone()
-    out = sdm.sdm_forward(sh_g, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M)
     o = sdm.sdm_rmsnorm_gate(sh_g, out["y"], gate.to(DEV), out_dtype=sdm.SDM_F32)
     status_ok()
-    ref = O.forward(sh_o, *(np32(x[k]) for k in ("q_w", "q_r", "K", "alpha", "beta", "v")),
-                    x["M0"].numpy())
-    if np.array_equal(out["idx_w"].cpu().numpy(), ref["idx_w"]) and \
-            np.array_equal(out["idx_r"].cpu().numpy(), ref["idx_r"]):
-        ro = O.rmsnorm_gate(sh_o, ref["y"], np32(gate), eps=1e-6)
-        assert max_rel(np32(o), ro) <= FTOL
+    ro = O.rmsnorm_gate(sh_o, yo, np32(gate), eps=1e-6)
+    assert max_rel(np32(o), ro) <= FTOL
 
 
 # ------------------------------------------------------------------ decode
@@ -622,10 +644,9 @@ def test_decode_matches_oracle(case, epi):
     iw, ir = out["idx_w"].cpu().numpy(), out["idx_r"].cpu().numpy()
     check_indices(iw, ow[0], S_w, s)
     check_indices(ir, orr[0], S_r, s)
-    ww, wr = np32(out["wt_w"]).astype(np.float64), np32(out["wt_r"]).astype(np.float64)
-    same = np.all(iw == ow[0], axis=-1) & np.all(ir == orr[0], axis=-1)
-    assert np.max(np.abs(ww[same] - ow[2][same]), initial=0) < 1e-5
-    # The scan part, on the device's own selections.
+    # The scan part, on the device's own selections with the oracle's weights
+    # for them (the device's weights checked on every row).
+    ww, wr = oracle_weights(sh_o, S_w, S_r, iw, ir, np32(out["wt_w"]), np32(out["wt_r"]))
     rows, Mo, yo = compact_oracle_scan(iw, ww, ir, wr, np32(x["alpha"]), np32(x["beta"]),
                                        np32(v), M0, form)
     assert max_rel(np32(out["y"]), yo) <= FTOL

@@ -4,7 +4,9 @@ benchmark times, checked on samples the oracle computes one by one:
 * addressing of a random sample of (b, h, t) tokens (the oracle's sub-scores
   and selection for just those tokens);
 * the whole recurrence of sampled chains (b, h), with the oracle scan fed the
-  device's selections and weights (addressing is checked separately);
+  device's selections and the oracle's own weights for them (the softmax of
+  its own sums of those slots; the device's weights are checked against them
+  on every token of the chain);
 * rows that no step of a chain wrote are bit-identical to M_0 (all chains).
 """
 import numpy as np
@@ -13,7 +15,7 @@ import torch
 
 import oracle as O
 from tests._helpers import (FTOL, check_indices, compact_oracle_scan, gshape, max_rel, np32,
-                           oshape)
+                           oracle_weights, oshape)
 from workloads import ORDER, WORKLOADS, generate
 
 pytestmark = pytest.mark.gpu
@@ -65,16 +67,31 @@ def test_fullsize_forward_sampled(name):
         # Differences are allowed only inside the 1e-5 score gap (asserted inside).
         check_indices(gw, ow[0], S_w, w.n_sub)
         check_indices(gr, orr[0], S_r, w.n_sub)
-        same = np.all(gw == ow[0], axis=-1)
-        assert np.max(np.abs(ww[bs[sel], h, ts[sel]][None, None][same] - ow[2][same])) < 1e-5
+        oracle_weights(sub, S_w, S_r, gw, gr, ww[bs[sel], h, ts[sel]][None, None],
+                       wr[bs[sel], h, ts[sel]][None, None])
 
     # Whole chains: the oracle recurrence on the device's selections.
     Mg = M  # updated in place on the device
     chains = [(0, 0), (w.B - 1, w.H - 1)] if w.B * w.H > 1 else [(0, 0)]
     for b, h in chains:
-        one = O.Shape(B=1, H=1, T=w.T, n_sub=w.n_sub, d_h=w.d_h, d_v=w.d_v, W=w.W, R=w.R)
-        Mo, yo = O.scan(one, iw[b:b + 1, h:h + 1], ww[b:b + 1, h:h + 1].astype(np.float64),
-                        ir[b:b + 1, h:h + 1], wr[b:b + 1, h:h + 1].astype(np.float64),
+        one = O.Shape(B=1, H=1, T=w.T, n_sub=w.n_sub, d_h=w.d_h, d_v=w.d_v, W=w.W, R=w.R,
+                      k_w=w.k_w, k_r=w.k_r, score_kind=w.score_kind, idw_eps=w.idw_eps)
+        K = np32(x["K"][h:h + 1])
+        S_w = O.subscores(one, np32(x["q_w"][b:b + 1, h:h + 1]), K)
+        S_r = O.subscores(one, np32(x["q_r"][b:b + 1, h:h + 1]), K)
+        cw, cr = iw[b:b + 1, h:h + 1], ir[b:b + 1, h:h + 1]
+        # The chain's selections against the oracle's on every token (every
+        # 16th token of the long sequence, to bound the oracle's sorting).
+        st = 16 if w.T > 16384 else 1
+        sub = O.Shape(B=1, H=1, T=len(range(0, w.T, st)), n_sub=w.n_sub, d_h=w.d_h,
+                      d_v=w.d_v, W=w.W, R=w.R, k_w=w.k_w, k_r=w.k_r)
+        check_indices(cw[:, :, ::st], O.select(sub, 0, S_w[:, :, ::st])[0], S_w[:, :, ::st],
+                      w.n_sub)
+        check_indices(cr[:, :, ::st], O.select(sub, 1, S_r[:, :, ::st])[0], S_r[:, :, ::st],
+                      w.n_sub)
+        ow_c, or_c = oracle_weights(one, S_w, S_r, cw, cr, ww[b:b + 1, h:h + 1],
+                                    wr[b:b + 1, h:h + 1])
+        Mo, yo = O.scan(one, cw, ow_c, cr, or_c,
                         np32(x["alpha"][b:b + 1, h:h + 1]), np32(x["beta"][b:b + 1, h:h + 1]),
                         np32(x["v"][b:b + 1, h:h + 1]), x["M0"][b:b + 1, h:h + 1].numpy())
         yg = out["y"][b, h].cpu().numpy()
@@ -121,10 +138,9 @@ def test_fullsize_decode_sampled(name, epi):
     iw, ir = out["idx_w"].cpu().numpy(), out["idx_r"].cpu().numpy()
     check_indices(iw, ow[0], S_w, w.n_sub)
     check_indices(ir, orr[0], S_r, w.n_sub)
-    ww, wr = np32(out["wt_w"]).astype(np.float64), np32(out["wt_r"]).astype(np.float64)
     same = np.all(iw == ow[0], axis=-1) & np.all(ir == orr[0], axis=-1)
     assert same.mean() > 0.9
-    assert np.max(np.abs(ww[same] - ow[2][same]), initial=0) < 1e-5
+    ww, wr = oracle_weights(sh_o, S_w, S_r, iw, ir, np32(out["wt_w"]), np32(out["wt_r"]))
     rows, Mo, yo = compact_oracle_scan(iw, ww, ir, wr, np32(x["alpha"]), np32(x["beta"]),
                                        np32(x["v"]), M0, w.update_form)
     assert max_rel(np32(out["y"]), yo) <= FTOL

@@ -133,6 +133,61 @@ def test_weights_entropy_range(oracle_mod):
     assert np.all(u >= 1.0 / W - 1e-12) and np.all(u <= 1 + 1e-12)
 
 
+def test_slot_weights_worked_example(oracle_mod):
+    """SDM reading notes 2.3 example: weights of slots [0, 1] (sums 7, 6) are
+    e/(1+e) and 1/(1+e), in either list order; slot 5 (sum 1 + 2 = 3)
+    scores through half 1 entry 1 and half 2 entry 1."""
+    g = gold("pkm_addressing_example.json")
+    s = g["n_sub"]
+    S = np.array([g["half1"], g["half2"]], np.float32).reshape(1, 1, 1, 2, s)
+    shape = sh(n_sub=s, W=2, R=2)
+    e = math.e
+    wt = O.slot_weights(shape, 0, S, np.array([0, 1], np.int32).reshape(1, 1, 1, 2))
+    assert wt[0, 0, 0] == pytest.approx([e / (1 + e), 1 / (1 + e)], abs=1e-15)
+    wt = O.slot_weights(shape, 1, S, np.array([1, 0], np.int32).reshape(1, 1, 1, 2))
+    assert wt[0, 0, 0] == pytest.approx([1 / (1 + e), e / (1 + e)], abs=1e-15)
+    # Sums 7 (slot 0) and 3 (slot 5): weights 1/(1+e^-4) and e^-4/(1+e^-4).
+    wt = O.slot_weights(shape, 0, S, np.array([5, 0], np.int32).reshape(1, 1, 1, 2))
+    q = math.exp(-4.0)
+    assert wt[0, 0, 0] == pytest.approx([q / (1 + q), 1 / (1 + q)], abs=1e-15)
+
+
+def test_slot_weights_log_scores_normalise(oracle_mod):
+    """Half 1 all zero and half 2 entry b = ln(b + 1): the softmax of
+    ln(b + 1) over the listed slots is (b + 1) / sum(b + 1), whatever the
+    half-1 index; a swapped slot map (a = slot % s) would read zeros."""
+    s, n = 16, 7
+    rng = np.random.default_rng(11)
+    S = np.zeros((1, 1, 3, 2, s), np.float32)
+    S[..., 1, :] = np.log(np.arange(1, s + 1, dtype=np.float64)).astype(np.float32)
+    idx = np.stack([rng.choice(s * s, n, replace=False) for _ in range(3)]).astype(np.int32)
+    idx = idx.reshape(1, 1, 3, n)
+    wt = O.slot_weights(sh(T=3, n_sub=s, W=n, R=n), 0, S, idx)
+    b = (idx % s).astype(np.float64)
+    # Expected from the float32-rounded logs, so only the softmax is exercised.
+    ev = np.exp(S[0, 0, :, 1][np.arange(3)[:, None], idx[0, 0] % s].astype(np.float64))
+    assert np.allclose(wt[0, 0], ev / ev.sum(-1, keepdims=True), atol=1e-15, rtol=0)
+    assert np.allclose(wt[0, 0], (b + 1) / (b + 1).sum(-1, keepdims=True), atol=1e-6)
+
+
+def test_slot_weights_invariants(oracle_mod):
+    """Weights sum to 1, a single slot gets exactly 1, equal sums get exactly
+    1/n, and a slot outside the table is rejected."""
+    rng = np.random.default_rng(12)
+    s, T = 8, 20
+    S = rng.standard_normal((1, 1, T, 2, s)).astype(np.float32)
+    idx = np.stack([rng.choice(s * s, 8, replace=False) for _ in range(T)]).astype(np.int32)
+    wt = O.slot_weights(sh(T=T, n_sub=s, W=8, R=8), 0, S, idx.reshape(1, 1, T, 8))
+    assert np.all(np.abs(wt.sum(-1) - 1) < 1e-12) and np.all(wt > 0)
+    one = O.slot_weights(sh(T=T, n_sub=s, W=1, R=1), 1, S, idx[:, :1].reshape(1, 1, T, 1))
+    assert np.all(one == 1.0)
+    flat = np.full((1, 1, 1, 2, s), 0.25, np.float32)
+    eq = O.slot_weights(sh(n_sub=s, W=4, R=4), 0, flat, np.array([[[[3, 9, 60, 1]]]], np.int32))
+    assert np.all(eq == 0.25)
+    with pytest.raises(ValueError):
+        O.slot_weights(sh(n_sub=s, W=1, R=1), 0, flat, np.array([[[[s * s]]]], np.int32))
+
+
 def test_permuting_subkeys_permutes_slots(oracle_mod):
     rng = np.random.default_rng(6)
     s, dh, W = 16, 8, 8

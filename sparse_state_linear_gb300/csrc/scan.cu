@@ -128,8 +128,11 @@ struct Ring {
   }
 };
 
-template <int CW, bool BF16, bool FIG2>
-__global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
+// MINB: CTAs per SM the launch is sized for (2 on the bandwidth-bound
+// workloads; 1 where every unit has an SM of its own and the per-step
+// latency decides, which leaves the compiler twice the registers).
+template <int CW, bool BF16, bool FIG2, bool UNDO, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) scan_kernel(const ScanArgs A) {
   constexpr int CH = CW / 4;               // 16-byte chunks per row slice
   constexpr int RP = kConsumers / CH;      // rows per consumer pass
   constexpr int IB = BF16 ? 2 : 4;         // input element bytes
@@ -277,18 +280,20 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
     float* Ml = Mc + 4 * lc;
     unsigned char* sm_l = smem + 16 * lc;
     Ring mu{0, MR, 0u}, me{0, MR, 0u}, rf{0, D, 0u}, lw{0, NS, 0u};
-    bool ok = true;
-    for (int u = 0; u < T && ok; ++u) {
-      if (lane == 0)
-        ok = u >= D ? mbar_wait2_bounded(&mfull[mu.i], mu.phase, &mempty[me.i], me.phase,
-                                         kTimeoutNs)
-                    : mbar_wait_bounded(&mfull[mu.i], mu.phase, kTimeoutNs);
-      __syncwarp();
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);
-        break;
+    for (int u = 0; u < T; ++u) {
+      // One thread waits for the step's metadata and for step u - D; the
+      // other loaders sleep in a named barrier meanwhile (which also orders
+      // their reads after that thread's acquire).  Waiting here is off the
+      // critical path (the loaders run depth steps ahead), so it suspends.
+      bool failed = false;
+      if (lt == 0) {
+        bool ok = u >= D ? mbar_wait2_bounded(&mfull[mu.i], mu.phase, &mempty[me.i], me.phase,
+                                              kTimeoutNs)
+                         : mbar_wait_bounded(&mfull[mu.i], mu.phase, kTimeoutNs);
+        if (!ok) record_status(A.status, SDM_ERR_TIMEOUT);
+        failed = !ok;
       }
+      if (named_bar_or(3, kLoaders, failed)) break;
       const MetaSlot* m = meta + mu.i;
       // Only rows whose current value is in HBM (code -1) are fetched; a
       // forwarded (>= 0) or invalid (-2) row is not.
@@ -382,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
             const int sl = wt.i >= dd ? wt.i - dd : wt.i - dd + NS;
             md[i] = *reinterpret_cast<const float4*>(tile_chunk(sl, p, cc));
           }
-          if (A.undo)
+          if constexpr (UNDO)
             *reinterpret_cast<float4*>(A.undo + ((th0 + t) * W + j) * dv + c0 + 4 * cc) = md[i];
           md[i] = make_float4(a * md[i].x, a * md[i].y, a * md[i].z, a * md[i].w);
           part.x = fmaf(wj[i], md[i].x, part.x);
@@ -522,6 +527,152 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
       *reinterpret_cast<float4*>(ypart + (tp & 1) * 8 * CW + warp * CW + 4 * lane) = acc;
   };
 
+  if constexpr (!FIG2) {
+    // Eq. (4).  The loop keeps its per-step work to the minimum: the ring
+    // positions of the step advance as pointers, every per-thread offset is
+    // computed once, and rows a thread does not hold are masked instead of
+    // branched around.
+    const MetaSlot* m = meta;                  // metadata slot of step t
+    int mi = 0;
+    unsigned mph = 0u;
+    unsigned char* const wt0 = sm_c + L.wtile;
+    unsigned char* wcur = wt0;                 // write tile of step t
+    int wi = 0;                                // its slot
+    const unsigned char* const rt0 = sm_c + L.rtile;
+    const unsigned char* rcur = rt0;           // read tile of step t
+    int ri = 0;
+    unsigned rph = 0u;
+    float* undo_p = nullptr;                   // log row of (t, j = myr)
+    if constexpr (UNDO) undo_p = A.undo + (th0 * W + myr) * dv + c0 + 4 * myc;
+    const size_t undo_step = (size_t)W * dv;
+    // On-chip copy of a forwarded row: position p of the write tile of step
+    // t - dd, for plan code (dd << 6) | p.
+    // (Slot arithmetic on indices: a shared-memory pointer must not step
+    // below the window even transiently.)
+    auto fwd = [&](int code) -> const float4* {
+      int sl = wi - (code >> 6);
+      if (sl < 0) sl += NS;
+      return reinterpret_cast<const float4*>(wt0 + sl * wslot + (code & 63) * rowb);
+    };
+    for (int t = 0; t < T; ++t) {
+      // Rows and metadata of step t: every lane tests both barriers, the
+      // previous step's read sum is reduced meanwhile.
+      {
+        const bool r0 = mbar_test_wait(&rfull[ri], rph);
+        const bool m0 = mbar_test_wait(&mfull[mi], mph);
+        if (t > 0) store_partial(t - 1, acc_prev);
+        if (!__all_sync(0xffffffffu, r0 && m0)) {
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait2_bounded(&rfull[ri], rph, &mfull[mi], mph, kTimeoutNs);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);
+            aborted = true;
+          }
+        }
+      }
+      if (!aborted) {
+        // Write: decay + per-slot delta (Eq. (3)-(4)).  Every row this thread
+        // writes is read first, so the rows' shared-memory latencies overlap.
+        const float a = m->alpha, b = m->beta;
+        const float4 vv = load_v4<BF16>(m->vraw, myc);
+        int code[kMaxPW], row[kMaxPW];
+        float wj[kMaxPW];
+        float4 x[kMaxPW];
+#pragma unroll
+        for (int pw = 0; pw < kMaxPW; ++pw) {
+          const int j = pw * RP + myr;
+          code[pw] = -2;
+          if (pw * RP < W - myr) {
+            code[pw] = m->code[j];
+            row[pw] = m->idx_w[j];
+            wj[pw] = m->wt_w[j];
+            x[pw] = *reinterpret_cast<const float4*>(wcur + j * rowb);   // fetched copy
+          }
+        }
+#pragma unroll
+        for (int pw = 0; pw < kMaxPW; ++pw) {
+          const int j = pw * RP + myr;
+          if (code[pw] >= 0) x[pw] = *fwd(code[pw]);
+          const bool live = code[pw] != -2;                              // absent / invalid
+          if constexpr (UNDO) {
+            if (live) *reinterpret_cast<float4*>(undo_p + (size_t)pw * RP * dv) = x[pw];
+          }
+          const float cw = b * wj[pw];
+          float4 o;
+          float mt_;
+          mt_ = a * x[pw].x; o.x = fmaf(cw, vv.x - mt_, mt_);
+          mt_ = a * x[pw].y; o.y = fmaf(cw, vv.y - mt_, mt_);
+          mt_ = a * x[pw].z; o.z = fmaf(cw, vv.z - mt_, mt_);
+          mt_ = a * x[pw].w; o.w = fmaf(cw, vv.w - mt_, mt_);
+          if (live) {
+            *reinterpret_cast<float4*>(wcur + j * rowb) = o;
+            *reinterpret_cast<float4*>(Mt + (size_t)row[pw] * dv) = o;
+          }
+        }
+      }
+      // The one block barrier of a step; it also turns a timeout anywhere
+      // into a decision every consumer takes at the same point.
+      if (named_bar_or(1, kConsumers, aborted)) {
+        aborted = true;
+        break;
+      }
+      if (t > 0 && warp == ((t - 1) & 7)) finalize(t - 1);
+      // Read after the write (Eq. (5)); all of this thread's rows are read first.
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      {
+        int code[kMaxPR];
+        float w[kMaxPR];
+        float4 xr[kMaxPR];
+#pragma unroll
+        for (int pr = 0; pr < kMaxPR; ++pr) {
+          const int q = pr * RP + myr;
+          code[pr] = -2;
+          if (pr * RP < R - myr) {
+            code[pr] = m->code[W + q];
+            w[pr] = m->wt_r[q];
+            xr[pr] = *reinterpret_cast<const float4*>(rcur + q * rowb);
+          }
+        }
+#pragma unroll
+        for (int pr = 0; pr < kMaxPR; ++pr) {
+          if (code[pr] == -2) continue;                                  // absent / invalid
+          if (code[pr] >= 0) xr[pr] = *fwd(code[pr]);
+          acc.x = fmaf(w[pr], xr[pr].x, acc.x);
+          acc.y = fmaf(w[pr], xr[pr].y, acc.y);
+          acc.z = fmaf(w[pr], xr[pr].z, acc.z);
+          acc.w = fmaf(w[pr], xr[pr].w, acc.w);
+        }
+      }
+      acc_prev = acc;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mempty[mi]);
+      // Next step's ring positions.
+      if (++mi == MR) {
+        mi = 0;
+        mph ^= 1u;
+        m = meta;
+      } else {
+        ++m;
+      }
+      wcur += wslot;
+      if (++wi == NS) {
+        wi = 0;
+        wcur = wt0;
+      }
+      rcur += rslot;
+      if (++ri == D) {
+        ri = 0;
+        rph ^= 1u;
+        rcur = rt0;
+      }
+      if constexpr (UNDO) undo_p += undo_step;
+    }
+    if (T > 0) store_partial(T - 1, acc_prev);
+    named_bar_sync(1, kConsumers);
+    if (!aborted && T > 0 && warp == ((T - 1) & 7)) finalize(T - 1);
+    return;
+  }
+
   for (int t = 0; t < T; ++t) {
     // Rows of step t landed (and its metadata is decoded): every lane tests
     // both barriers; the previous step's read sum is reduced meanwhile.
@@ -566,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
         const int j = pw * RP + myr;
         if (code[pw] == -2) continue;                                   // absent / invalid
         if (code[pw] >= 0) x[pw] = *reinterpret_cast<const float4*>(fwd_place(code[pw], wt.i));
-        if (A.undo)
+        if constexpr (UNDO)
           *reinterpret_cast<float4*>(A.undo + ((th0 + t) * W + j) * dv + c0 + 4 * myc) = x[pw];
         const float cw = b * wj[pw];
         float4 o;
@@ -596,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
           float4 x = *reinterpret_cast<const float4*>(wdst + j * rowb);
           if (code == -2) continue;
           if (code >= 0) x = *reinterpret_cast<const float4*>(fwd_place(code, wt.i));
-          if (A.undo)
+          if constexpr (UNDO)
             *reinterpret_cast<float4*>(A.undo + ((th0 + t) * W + j) * dv + c0 + 4 * myc) = x;
           const float wj = m->wt_w[j];
           md[pw] = make_float4(a * x.x, a * x.y, a * x.z, a * x.w);
@@ -696,10 +847,13 @@ __global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs A) {
 }
 
 template <int CW, bool BF16>
-cudaError_t launch_t(const ScanArgs& A, cudaStream_t stream) {
+cudaError_t launch_t(const ScanArgs& A, bool one_per_sm, cudaStream_t stream) {
   const size_t smem = scan_layout(CW, A.d.W, A.d.R, A.depth).total;
-  auto kfn = A.d.update == SDM_UPDATE_SHARED_RESIDUAL ? scan_kernel<CW, BF16, true>
-                                                      : scan_kernel<CW, BF16, false>;
+  const bool fig2 = A.d.update == SDM_UPDATE_SHARED_RESIDUAL, logged = A.undo != nullptr;
+  auto kfn = fig2 ? (logged ? scan_kernel<CW, BF16, true, true, 2> : scan_kernel<CW, BF16, true, false, 2>)
+                  : (logged ? scan_kernel<CW, BF16, false, true, 2>
+                            : (one_per_sm ? scan_kernel<CW, BF16, false, false, 1>
+                                          : scan_kernel<CW, BF16, false, false, 2>));
   cudaError_t e =
       cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -749,9 +903,10 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   if (e != cudaSuccess) return e;
   ScanArgs A{d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, codes, M, y, undo, D, status};
   const bool bf = d.in_dtype == SDM_BF16;
-  if (cw == 64) return bf ? launch_t<64, true>(A, stream) : launch_t<64, false>(A, stream);
-  if (cw == 32) return bf ? launch_t<32, true>(A, stream) : launch_t<32, false>(A, stream);
-  return bf ? launch_t<16, true>(A, stream) : launch_t<16, false>(A, stream);
+  const bool one = per_sm <= 1;
+  if (cw == 64) return bf ? launch_t<64, true>(A, one, stream) : launch_t<64, false>(A, one, stream);
+  if (cw == 32) return bf ? launch_t<32, true>(A, one, stream) : launch_t<32, false>(A, one, stream);
+  return bf ? launch_t<16, true>(A, one, stream) : launch_t<16, false>(A, one, stream);
 }
 
 }  // namespace sdm

@@ -294,9 +294,19 @@ __device__ bool warp_topk_bucketed(const Src& src, int n, int k, WarpScratch& ws
     h4[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncwarp();
+  // Each element's arrival order within its bucket (the count before its
+  // own increment) places it in bucket order later without a second pass of
+  // atomics; the orders are kept as bytes, four to a register.
+  constexpr int PW = (PL + 3) / 4;
+  uint32_t ord[PW];
+#pragma unroll
+  for (int i = 0; i < PW; ++i) ord[i] = 0u;
 #pragma unroll
   for (int i = 0; i < PL; ++i)
-    if (lane + 32 * i < n) atomicAdd(&ws.hist[bucket(v[i])], 1u);
+    if (lane + 32 * i < n) {
+      const uint32_t o = atomicAdd(&ws.hist[bucket(v[i])], 1u);
+      ord[i >> 2] |= (o & 255u) << (8 * (i & 3));
+    }
   __syncwarp();
   // Exclusive prefix over buckets (lane owns 8 consecutive buckets).
   uint32_t c[8], tot = 0;
@@ -325,13 +335,11 @@ __device__ bool warp_topk_bucketed(const Src& src, int n, int k, WarpScratch& ws
     run += c[i];
   }
   {
-    // Bucket bases; the histogram becomes the scatter cursors.
+    // Bucket bases.
     const uint4 a = make_uint4(pre[0], pre[1], pre[2], pre[3]);
     const uint4 b = make_uint4(pre[4], pre[5], pre[6], pre[7]);
     reinterpret_cast<uint4*>(ws.base)[2 * lane] = a;
     reinterpret_cast<uint4*>(ws.base)[2 * lane + 1] = b;
-    reinterpret_cast<uint4*>(ws.hist)[2 * lane] = a;
-    reinterpret_cast<uint4*>(ws.hist)[2 * lane + 1] = b;
   }
   if (lane == 31) ws.base[256] = run;
 #pragma unroll
@@ -339,19 +347,17 @@ __device__ bool warp_topk_bucketed(const Src& src, int n, int k, WarpScratch& ws
   __syncwarp();
   const uint32_t ncand = ws.base[bstar + 1];
   if (ncand > (uint32_t)kTmpCap) return false;
-  // Scatter the candidates in bucket order.
+  // Scatter the candidates in bucket order: bucket base + arrival order
+  // (counts never exceed n < 256 per bucket, so a byte holds the order).
 #pragma unroll
   for (int i = 0; i < PL; ++i) {
     const int e = lane + 32 * i;
     if (e < n) {
       const uint32_t b = bucket(v[i]);
       if (b <= bstar) {
-        float vv;
-        uint32_t id;
-        src.get(e, vv, id);
-        const uint32_t pos = atomicAdd(&ws.hist[b], 1u);
+        const uint32_t pos = ws.base[b] + ((ord[i >> 2] >> (8 * (i & 3))) & 255u);
         ws.tmp_v[pos] = v[i];
-        ws.tmp_id[pos] = id;
+        ws.tmp_id[pos] = src.id(e);
       }
     }
   }
@@ -389,6 +395,7 @@ struct RowSrc {
     v = row[e];
     id = (uint32_t)e;
   }
+  __device__ __forceinline__ uint32_t id(int e) const { return (uint32_t)e; }
 };
 
 // Candidate pairs (a, b) listed in `pairs` as (a << 8) | b.
@@ -405,6 +412,10 @@ struct PairSrc {
     v = __fadd_rn(v1[a], v2[b]);
     id = id1[a] * s + id2[b];
   }
+  __device__ __forceinline__ uint32_t id(int e) const {
+    const uint32_t ab = pairs[e];
+    return id1[ab >> 8] * s + id2[ab & 255u];
+  }
 };
 
 // The full k x k grid, element e = a*k + b.
@@ -419,6 +430,10 @@ struct GridSrc {
     const int a = e / k, b = e - a * k;
     v = __fadd_rn(v1[a], v2[b]);
     id = id1[a] * s + id2[b];
+  }
+  __device__ __forceinline__ uint32_t id(int e) const {
+    const int a = e / k, b = e - a * k;
+    return id1[a] * s + id2[b];
   }
 };
 

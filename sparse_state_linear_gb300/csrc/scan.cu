@@ -51,7 +51,13 @@ namespace {
 constexpr int kConsumers = 256;
 constexpr int kLoaders = 128;    // loader threads (4 warps) that fetch the rows
 constexpr int kThreads = kConsumers + 32 + kLoaders;
-constexpr int kP = 4;            // producer's metadata prefetch distance (steps)
+// Producer's metadata prefetch distance (steps): the copies of a step are
+// waited for kP steps after they were issued, so at most kP steps' metadata
+// is in flight; their latency (microseconds under load) over kP bounds the
+// step rate.  Deep where a CTA has an SM of its own (shared memory to
+// spare), shallow where two CTAs share one.
+template <int MINB>
+__host__ __device__ constexpr int prefetch_steps() { return MINB == 1 ? 16 : 4; }
 constexpr int kSlack = 4;        // steps the producer may prepare beyond the need
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 
@@ -90,7 +96,7 @@ struct ScanLayout {
   int NS, MR;
 };
 
-__host__ __device__ inline ScanLayout scan_layout(int CW, int W, int R, int D) {
+__host__ __device__ inline ScanLayout scan_layout(int CW, int W, int R, int D, int kP) {
   ScanLayout L;
   L.NS = 2 * D;
   L.MR = D + kP + 1 + kSlack;
@@ -146,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, MINB) scan_kernel(const ScanArgs A) 
   const Dims& d = A.d;
   const int D = A.depth;
   const int W = d.W, R = d.R, T = d.T, dv = d.dv;
-  const ScanLayout L = scan_layout(CW, W, R, D);
+  const ScanLayout L = scan_layout(CW, W, R, D, prefetch_steps<MINB>());
   const int NS = L.NS, MR = L.MR;
   const int nslice = dv / CW;
   const int chain = blockIdx.x / nslice;
@@ -191,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, MINB) scan_kernel(const ScanArgs A) 
     const bool vec = (W & 3) == 0 && (R & 3) == 0;
     const uint32_t vbytes = (uint32_t)(CW * IB);
     Ring mi{0, MR, 0u};         // slot of step u (copy stage)
+    constexpr int kP = prefetch_steps<MINB>();
     Ring mp{0, MR, 0u};         // slot of step up = u - kP (publish stage)
     bool failed = false;
     for (int u = 0; u < T + kP && !failed; ++u) {
@@ -848,8 +855,9 @@ __global__ void __launch_bounds__(kThreads, MINB) scan_kernel(const ScanArgs A) 
 
 template <int CW, bool BF16>
 cudaError_t launch_t(const ScanArgs& A, bool one_per_sm, cudaStream_t stream) {
-  const size_t smem = scan_layout(CW, A.d.W, A.d.R, A.depth).total;
   const bool fig2 = A.d.update == SDM_UPDATE_SHARED_RESIDUAL, logged = A.undo != nullptr;
+  const int kp = one_per_sm && !fig2 && !logged ? prefetch_steps<1>() : prefetch_steps<2>();
+  const size_t smem = scan_layout(CW, A.d.W, A.d.R, A.depth, kp).total;
   auto kfn = fig2 ? (logged ? scan_kernel<CW, BF16, true, true, 2> : scan_kernel<CW, BF16, true, false, 2>)
                   : (logged ? scan_kernel<CW, BF16, false, true, 2>
                             : (one_per_sm ? scan_kernel<CW, BF16, false, false, 1>
@@ -885,6 +893,10 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   const long long units = chains * (d.dv / cw);
   // CTAs per SM needed to keep every unit resident, and the ring depth that fits.
   const long long per_sm = (units + sms - 1) / sms;
+  // The build that runs (see launch_t) and its metadata prefetch distance.
+  const bool one = per_sm <= 1;
+  const int kp = one && d.update != SDM_UPDATE_SHARED_RESIDUAL && !undo ? prefetch_steps<1>()
+                                                                        : prefetch_steps<2>();
   const size_t budget = per_sm <= 1    ? lim.smem_per_cta
                         : per_sm == 2 ? lim.smem_per_sm / 2 - 1024
                                       : lim.smem_per_sm / 3 - 1024;
@@ -892,18 +904,17 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   if (D == 0) {
     D = 1;
     for (int cand = 2; cand <= 16; ++cand)
-      if (scan_layout(cw, d.W, d.R, cand).total <= budget) D = cand;
+      if (scan_layout(cw, d.W, d.R, cand, kp).total <= budget) D = cand;
   }
   if (D < 1 || D > 16) return cudaErrorInvalidValue;
   // A requested depth is a hint: shrink it until the ring fits on chip.
-  while (D > 1 && scan_layout(cw, d.W, d.R, D).total > lim.smem_per_cta) --D;
+  while (D > 1 && scan_layout(cw, d.W, d.R, D, kp).total > lim.smem_per_cta) --D;
 
   int16_t* codes = static_cast<int16_t*>(workspace);
   cudaError_t e = launch_plan(d, idx_w, idx_r, codes, D, status, stream);
   if (e != cudaSuccess) return e;
   ScanArgs A{d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, codes, M, y, undo, D, status};
   const bool bf = d.in_dtype == SDM_BF16;
-  const bool one = per_sm <= 1;
   if (cw == 64) return bf ? launch_t<64, true>(A, one, stream) : launch_t<64, false>(A, one, stream);
   if (cw == 32) return bf ? launch_t<32, true>(A, one, stream) : launch_t<32, false>(A, one, stream);
   return bf ? launch_t<16, true>(A, one, stream) : launch_t<16, false>(A, one, stream);

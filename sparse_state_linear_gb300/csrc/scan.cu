@@ -58,6 +58,7 @@ constexpr int kThreads = kConsumers + 32 + kLoaders;
 // spare), shallow where two CTAs share one.
 template <int MINB>
 __host__ __device__ constexpr int prefetch_steps() { return MINB == 1 ? 16 : 4; }
+constexpr int kPrefetchBatch = 4;   // steps the producer handles per loop pass
 constexpr int kSlack = 4;        // steps the producer may prepare beyond the need
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 
@@ -99,7 +100,7 @@ struct ScanLayout {
 __host__ __device__ inline ScanLayout scan_layout(int CW, int W, int R, int D, int kP) {
   ScanLayout L;
   L.NS = 2 * D;
-  L.MR = D + kP + 1 + kSlack;
+  L.MR = D + kP + kPrefetchBatch + kSlack;
   size_t o = 0;
   L.meta = o;  o += sizeof(MetaSlot) * L.MR;
   L.wtile = o; o += sizeof(float) * (size_t)L.NS * W * CW;
@@ -191,23 +192,75 @@ __global__ void __launch_bounds__(kThreads, MINB) scan_kernel(const ScanArgs A) 
       ga_nxt = load_scalar(A.alpha, th0 + 32 + lane, d.in_dtype);
       gb_nxt = load_scalar(A.beta, th0 + 32 + lane, d.in_dtype);
     }
-    // Slot lists, weights, codes and the value slice of step u: 16-byte
-    // cp.async when every array is a whole number of 16-byte units, else
-    // 4-byte cp.async per element.
+    // Slot lists, weights, codes and the value slice of each step into its
+    // metadata slot, kPS steps per iteration (one slot wait, one commit
+    // group, one group wait and one loop pass per batch).  With every array
+    // a whole number of 16-byte units each lane owns up to three fixed
+    // (array, chunk) copy jobs whose source pointers just advance by the
+    // array's step stride; otherwise 4-byte cp.async per element.
+    constexpr int kP = prefetch_steps<MINB>();
+    constexpr int kPS = kPrefetchBatch;
+    constexpr int kPB = kP / kPS;                // batches of copies in flight
+    static_assert(kP % kPS == 0 && 32 % kPS == 0, "prefetch batches");
     const bool vec = (W & 3) == 0 && (R & 3) == 0;
     const uint32_t vbytes = (uint32_t)(CW * IB);
+    const unsigned char* jsrc[3];
+    uint32_t jstride[3], jdst[3];
+    bool jlive[3];
+    {
+      const int n0 = W / 4, n1 = n0 + W / 4, n2 = n1 + R / 4, n3 = n2 + R / 4;
+      const int n4 = n3 + CP / 8, n5 = n4 + (int)vbytes / 16;
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const int j = lane + 32 * k;
+        jlive[k] = vec && j < n5;
+        const unsigned char* src = nullptr;
+        uint32_t stride = 0, dst = 0;
+        if (j < n0) {
+          src = reinterpret_cast<const unsigned char*>(A.idx_w + th0 * W + 4 * j);
+          stride = 4u * W;
+          dst = (uint32_t)offsetof(MetaSlot, idx_w) + 16u * j;
+        } else if (j < n1) {
+          src = reinterpret_cast<const unsigned char*>(A.wt_w + th0 * W + 4 * (j - n0));
+          stride = 4u * W;
+          dst = (uint32_t)offsetof(MetaSlot, wt_w) + 16u * (j - n0);
+        } else if (j < n2) {
+          src = reinterpret_cast<const unsigned char*>(A.idx_r + th0 * R + 4 * (j - n1));
+          stride = 4u * R;
+          dst = (uint32_t)offsetof(MetaSlot, idx_r) + 16u * (j - n1);
+        } else if (j < n3) {
+          src = reinterpret_cast<const unsigned char*>(A.wt_r + th0 * R + 4 * (j - n2));
+          stride = 4u * R;
+          dst = (uint32_t)offsetof(MetaSlot, wt_r) + 16u * (j - n2);
+        } else if (j < n4) {
+          src = reinterpret_cast<const unsigned char*>(A.codes + th0 * CP + 8 * (j - n3));
+          stride = 2u * CP;
+          dst = (uint32_t)offsetof(MetaSlot, code) + 16u * (j - n3);
+        } else if (j < n5) {
+          src = reinterpret_cast<const unsigned char*>(A.v) + (th0 * dv + c0) * IB + 16 * (j - n4);
+          stride = (uint32_t)(dv * IB);
+          dst = (uint32_t)offsetof(MetaSlot, vraw) + 16u * (j - n4);
+        }
+        jsrc[k] = src;
+        jstride[k] = stride;
+        jdst[k] = dst;
+      }
+    }
     Ring mi{0, MR, 0u};         // slot of step u (copy stage)
-    constexpr int kP = prefetch_steps<MINB>();
-    Ring mp{0, MR, 0u};         // slot of step up = u - kP (publish stage)
+    Ring mw{0, MR, 0u};         // slot of the batch's last step (slot-reuse wait)
+    Ring mp{0, MR, 0u};         // slot of step up (publish stage)
+    for (int i = 0; i < kPS - 1; ++i) mw.next();
     bool failed = false;
-    for (int u = 0; u < T + kP && !failed; ++u) {
-      if (u < T) {
-        if (u >= MR) {
-          // Slot reuse: step u - MR must be finished by the consumers.
-          bool ok = mbar_try_wait(&mempty[mi.i], mi.phase ^ 1u);
+    for (int u0 = 0; u0 < T + kP && !failed; u0 += kPS) {
+      if (u0 < T) {
+        // Slot reuse: the batch's last step reuses the slot of step
+        // u0 + kPS - 1 - MR; steps complete in order, so that one being
+        // finished frees every slot of the batch.
+        if (u0 + kPS - 1 >= MR) {
+          bool ok = mbar_try_wait(&mempty[mw.i], mw.phase ^ 1u);
           if (!ok) {
             const uint64_t t0 = global_ns();
-            while (!(ok = mbar_try_wait(&mempty[mi.i], mi.phase ^ 1u))) {
+            while (!(ok = mbar_try_wait(&mempty[mw.i], mw.phase ^ 1u))) {
               __nanosleep(64);
               if (global_ns() - t0 > kTimeoutNs) break;
             }
@@ -218,58 +271,68 @@ __global__ void __launch_bounds__(kThreads, MINB) scan_kernel(const ScanArgs A) 
             break;
           }
         }
-        MetaSlot* m = meta + mi.i;
-        const size_t th = th0 + u;
-        const unsigned char* vsrc =
-            reinterpret_cast<const unsigned char*>(A.v) + (th * dv + c0) * IB;
-        if (vec) {
-          for (int c = lane; c < W / 4; c += 32) {
-            cp_async16(&m->idx_w[4 * c], A.idx_w + th * W + 4 * c);
-            cp_async16(&m->wt_w[4 * c], A.wt_w + th * W + 4 * c);
-          }
-          for (int c = lane; c < R / 4; c += 32) {
-            cp_async16(&m->idx_r[4 * c], A.idx_r + th * R + 4 * c);
-            cp_async16(&m->wt_r[4 * c], A.wt_r + th * R + 4 * c);
-          }
-        } else {
-          for (int j = lane; j < W; j += 32) {
-            cp_async4(&m->idx_w[j], A.idx_w + th * W + j);
-            cp_async4(&m->wt_w[j], A.wt_w + th * W + j);
-          }
-          for (int j = lane; j < R; j += 32) {
-            cp_async4(&m->idx_r[j], A.idx_r + th * R + j);
-            cp_async4(&m->wt_r[j], A.wt_r + th * R + j);
+#pragma unroll
+        for (int s = 0; s < kPS; ++s) {
+          const int u = u0 + s;
+          if (u < T) {
+            unsigned char* m = reinterpret_cast<unsigned char*>(meta + mi.i);
+            if (vec) {
+#pragma unroll
+              for (int k = 0; k < 3; ++k) {
+                if (jlive[k]) cp_async16(m + jdst[k], jsrc[k]);
+                jsrc[k] += jstride[k];
+              }
+            } else {
+              MetaSlot* ms = meta + mi.i;
+              const size_t th = th0 + u;
+              for (int j = lane; j < W; j += 32) {
+                cp_async4(&ms->idx_w[j], A.idx_w + th * W + j);
+                cp_async4(&ms->wt_w[j], A.wt_w + th * W + j);
+              }
+              for (int j = lane; j < R; j += 32) {
+                cp_async4(&ms->idx_r[j], A.idx_r + th * R + j);
+                cp_async4(&ms->wt_r[j], A.wt_r + th * R + j);
+              }
+              if (lane < CP / 8) cp_async16(&ms->code[8 * lane], A.codes + th * CP + 8 * lane);
+              if (lane < (int)vbytes / 16)
+                cp_async16(ms->vraw + 16 * lane, reinterpret_cast<const unsigned char*>(A.v) +
+                                                     (th * dv + c0) * IB + 16 * lane);
+            }
+            mi.next();
           }
         }
-        if (lane < CP / 8) cp_async16(&m->code[8 * lane], A.codes + th * CP + 8 * lane);
-        if (lane < (int)vbytes / 16) cp_async16(m->vraw + 16 * lane, vsrc + 16 * lane);
-        mi.next();
+        for (int s = 0; s < kPS; ++s) mw.next();
       }
       cp_async_commit();
-      if (u < kP) continue;
+      if (u0 < kP) continue;
 
-      // ---- step up: its metadata has landed; add the gates and publish.
-      const int up = u - kP;
-      MetaSlot* m = meta + mp.i;
-      cp_async_wait<kP>();
+      // ---- batch up0 = u0 - kP: its metadata has landed; gates, publish.
+      const int up0 = u0 - kP;
+      cp_async_wait<kPB>();
       __syncwarp();
-      if ((up & 31) == 0 && up > 0) {
-        ga_cur = ga_nxt;
-        gb_cur = gb_nxt;
-        if (up + 32 + lane < T) {
-          ga_nxt = load_scalar(A.alpha, th0 + up + 32 + lane, d.in_dtype);
-          gb_nxt = load_scalar(A.beta, th0 + up + 32 + lane, d.in_dtype);
+#pragma unroll
+      for (int s = 0; s < kPS; ++s) {
+        const int up = up0 + s;
+        if (up >= T) break;
+        if ((up & 31) == 0 && up > 0) {
+          ga_cur = ga_nxt;
+          gb_cur = gb_nxt;
+          if (up + 32 + lane < T) {
+            ga_nxt = load_scalar(A.alpha, th0 + up + 32 + lane, d.in_dtype);
+            gb_nxt = load_scalar(A.beta, th0 + up + 32 + lane, d.in_dtype);
+          }
         }
+        const float ga = __shfl_sync(0xffffffffu, ga_cur, up & 31);
+        const float gb = __shfl_sync(0xffffffffu, gb_cur, up & 31);
+        MetaSlot* m = meta + mp.i;
+        if (lane == 0) {
+          m->alpha = ga;
+          m->beta = gb;
+        }
+        __syncwarp();
+        mbar_arrive(&mfull[mp.i]);
+        mp.next();
       }
-      const float ga = __shfl_sync(0xffffffffu, ga_cur, up & 31);
-      const float gb = __shfl_sync(0xffffffffu, gb_cur, up & 31);
-      if (lane == 0) {
-        m->alpha = ga;
-        m->beta = gb;
-      }
-      __syncwarp();
-      mbar_arrive(&mfull[mp.i]);
-      mp.next();
     }
     cp_async_wait_all();
     return;

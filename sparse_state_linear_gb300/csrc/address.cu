@@ -25,6 +25,10 @@ constexpr int kBN = 256;        // sub-key chunk
 constexpr int kThreads = 256;   // 8 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kStairMax = 320;  // >= sum_{a<64} floor(64/(a+1)) = 280
+// q tile row stride in (q, q) pairs: row r sits at r + 2 * (r / 16), so the
+// four 8-row groups a warp reads at once start in distinct bank quarters.
+constexpr int kQStride = kRows + 4;
+__host__ __device__ constexpr int qpos(int r) { return r + 2 * (r >> 4); }
 
 struct AddrArgs {
   Dims d;
@@ -43,24 +47,35 @@ struct AddrArgs {
 
 struct SmemLayout {
   size_t qT, kT, sc, lv, lid, ws, stair, nst, total;
+  int kst;                     // stride of one per-half list (>= k of both branches)
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout smem_layout(int s) {
+// The q / K tiles live only while scores are computed and the warps'
+// selection scratch only while rows are selected (a block barrier separates
+// the phases), so the two share one region; the per-half lists are as long
+// as the larger k.  At s = 512 and k = 8 this keeps a CTA near 100 KB, two
+// per SM.
+__host__ __device__ inline SmemLayout smem_layout(int s, int kmax) {
   SmemLayout L;
-  size_t o = 0;
-  L.qT = o;    o = align_up(o + sizeof(float) * kBK * kRows, 16);
-  L.kT = o;    o = align_up(o + sizeof(float) * kBK * kBN, 16);
+  L.kst = kmax;
+  L.qT = 0;
+  L.kT = align_up(sizeof(float2) * kBK * kQStride, 16);  // (q, q) pairs
+  const size_t tiles = L.kT + sizeof(float) * kBK * kBN;
+  L.ws = 0;
+  const size_t wsz = sizeof(WarpScratch) * kWarps;
+  size_t o = align_up(tiles > wsz ? tiles : wsz, 16);
   L.sc = o;    o = align_up(o + sizeof(float) * kRows * (size_t)s, 16);
-  L.lv = o;    o = align_up(o + sizeof(float) * kRows * 2 * kMaxSel, 16);
-  L.lid = o;   o = align_up(o + sizeof(uint32_t) * kRows * 2 * kMaxSel, 16);
-  L.ws = o;    o = align_up(o + sizeof(WarpScratch) * kWarps, 16);
+  L.lv = o;    o = align_up(o + sizeof(float) * kRows * 2 * (size_t)kmax, 16);
+  L.lid = o;   o = align_up(o + sizeof(uint32_t) * kRows * 2 * (size_t)kmax, 16);
   L.stair = o; o = align_up(o + sizeof(uint16_t) * 2 * kStairMax, 16);
   L.nst = o;   o = align_up(o + sizeof(int) * 2, 16);
   L.total = o;
   return L;
 }
+
+__host__ __device__ inline int list_len(const Dims& d) { return d.kw > d.kr ? d.kw : d.kr; }
 
 template <int MODE>
 __device__ __forceinline__ void row_item(int r, int& sigma, long long& item) {
@@ -73,15 +88,51 @@ __device__ __forceinline__ void row_item(int r, int& sigma, long long& item) {
   }
 }
 
-// Score tile of half p: rows x [j0, j0+kBN) accumulated over d_h.
+// Score tile of half p: rows x [j0, j0+kBN) accumulated over d_h.  The
+// (sub-key chunk, d chunk) tiles are walked as one sequence; the global
+// loads of the next tile are issued before the current tile's FMAs, so their
+// latency hides behind the contraction (raw words are kept in registers and
+// converted when they are stored to shared memory).
+// Packed pairs of fp32 lanes (two IEEE round-to-nearest operations per
+// instruction, each lane exactly what the scalar operation gives).
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f32x2_unpack(uint64_t v) {
+  float2 f;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+  return f;
+}
+
+template <bool BF16>
+struct TileRegs {
+  uint32_t q[2];             // this thread's two q elements (raw bits)
+  uint32_t k[kBK];           // its sub-key row's kBK elements (raw bits; bf16: 2 per word)
+};
+
 template <int MODE, bool BF16, int KIND>
-__device__ void score_half(const AddrArgs& A, int p, float* qT, float* kT, float* sc) {
+__device__ void score_half(const AddrArgs& A, int p, float2* qT, float* kT, float* sc) {
   const Dims& d = A.d;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.y;
   const long long BT = (long long)d.B * d.T;
-  const int rb = 8 * (warp & 3);
-  const int cb = 128 * (warp >> 2) + 4 * lane;
+  // Lane tile: 8 rows (group lane / 8) x 4 sub-keys; a warp covers all 32
+  // rows x 32 sub-keys, so per d step it reads four q pairs (one address per
+  // row group) and one 128-byte run of K.
+  const int rb = 8 * (lane >> 3);
+  const int cb = 32 * warp + 4 * (lane & 7);
 
   // Loader roles: q tile (row = tid/8, two d-elements), K tile (row jj = tid).
   const int lr = tid >> 3, lpart = tid & 7;
@@ -96,104 +147,122 @@ __device__ void score_half(const AddrArgs& A, int p, float* qT, float* kT, float
     qoff = (size_t)(th * 2 + p) * d.dh;
   }
   const void* qbase = (lsig == 0) ? A.q0 : A.q1;
+  const int nd = d.dh / kBK;
+  const int ntiles = ((d.s + kBN - 1) / kBN) * nd;
 
-  for (int j0 = 0; j0 < d.s; j0 += kBN) {
-    float acc[8][4];
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
-
-    for (int d0 = 0; d0 < d.dh; d0 += kBK) {
-      __syncthreads();
-      // q tile: qT[dd][row]
-      {
-        float x0 = 0.f, x1 = 0.f;
-        if (lvalid) {
-          const size_t e = qoff + d0 + 2 * lpart;
-          if (BF16) {
-            const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(
-                reinterpret_cast<const __nv_bfloat16*>(qbase) + e));
-            x0 = bf16_bits_to_float(w & 0xffffu);
-            x1 = bf16_bits_to_float(w >> 16);
-          } else {
-            const float2 w = __ldg(reinterpret_cast<const float2*>(
-                reinterpret_cast<const float*>(qbase) + e));
-            x0 = w.x;
-            x1 = w.y;
-          }
-        }
-        qT[(2 * lpart) * kRows + lr] = x0;
-        qT[(2 * lpart + 1) * kRows + lr] = x1;
-      }
-      // K tile: kT[dd][jj]
-      {
-        const int j = j0 + tid;
-        float x[kBK];
-        if (j < d.s) {
-          const size_t e = ((size_t)(h * 2 + p) * d.s + j) * d.dh + d0;
-          if (BF16) {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                reinterpret_cast<const __nv_bfloat16*>(A.K) + e);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const uint4 w = __ldg(src + u);
-              const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                x[8 * u + 2 * c] = bf16_bits_to_float(ws4[c] & 0xffffu);
-                x[8 * u + 2 * c + 1] = bf16_bits_to_float(ws4[c] >> 16);
-              }
-            }
-          } else {
-            const float4* src = reinterpret_cast<const float4*>(
-                reinterpret_cast<const float*>(A.K) + e);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float4 w = __ldg(src + u);
-              x[4 * u] = w.x;
-              x[4 * u + 1] = w.y;
-              x[4 * u + 2] = w.z;
-              x[4 * u + 3] = w.w;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kBK; ++c) x[c] = 0.f;
-        }
-#pragma unroll
-        for (int c = 0; c < kBK; ++c) kT[c * kBN + tid] = x[c];
-      }
-      __syncthreads();
-#pragma unroll
-      for (int dd = 0; dd < kBK; ++dd) {
-        const float4 qa = *reinterpret_cast<const float4*>(qT + dd * kRows + rb);
-        const float4 qb = *reinterpret_cast<const float4*>(qT + dd * kRows + rb + 4);
-        const float4 kk = *reinterpret_cast<const float4*>(kT + dd * kBN + cb);
-        const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-        const float kv[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if (KIND == SDM_SCORE_DOT) {
-              acc[r][c] = fmaf(qv[r], kv[c], acc[r][c]);
-            } else {
-              const float df = qv[r] - kv[c];
-              acc[r][c] = fmaf(df, df, acc[r][c]);
-            }
-          }
+  auto fetch = [&](int it, TileRegs<BF16>& g) {
+    const int j0 = (it / nd) * kBN, d0 = (it % nd) * kBK;
+    g.q[0] = g.q[1] = 0u;
+    if (lvalid) {
+      const size_t e = qoff + d0 + 2 * lpart;
+      if (BF16) {
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(
+            reinterpret_cast<const __nv_bfloat16*>(qbase) + e));
+        g.q[0] = w & 0xffffu;
+        g.q[1] = w >> 16;
+      } else {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(
+            reinterpret_cast<const float*>(qbase) + e));
+        g.q[0] = w.x;
+        g.q[1] = w.y;
       }
     }
-    // Epilogue.
+    const int j = j0 + tid;
+    if (j < d.s) {
+      const size_t e = ((size_t)(h * 2 + p) * d.s + j) * d.dh + d0;
+      if (BF16) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __nv_bfloat16*>(A.K) + e);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint4 w = __ldg(src + u);
+          g.k[4 * u + 0] = w.x; g.k[4 * u + 1] = w.y;
+          g.k[4 * u + 2] = w.z; g.k[4 * u + 3] = w.w;
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const float*>(A.K) + e);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 w = __ldg(src + u);
+          g.k[4 * u + 0] = w.x; g.k[4 * u + 1] = w.y;
+          g.k[4 * u + 2] = w.z; g.k[4 * u + 3] = w.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < kBK; ++c) g.k[c] = 0u;
+    }
+  };
+  // q tile: qT[dd][qpos(row)] as (q, q) pairs; K tile: kT[dd][jj].
+  auto put = [&](const TileRegs<BF16>& g) {
+    if (BF16) {
+      const float x0 = bf16_bits_to_float(g.q[0]), x1 = bf16_bits_to_float(g.q[1]);
+      qT[(2 * lpart) * kQStride + qpos(lr)] = make_float2(x0, x0);
+      qT[(2 * lpart + 1) * kQStride + qpos(lr)] = make_float2(x1, x1);
+#pragma unroll
+      for (int c = 0; c < kBK / 2; ++c) {
+        kT[(2 * c) * kBN + tid] = bf16_bits_to_float(g.k[c] & 0xffffu);
+        kT[(2 * c + 1) * kBN + tid] = bf16_bits_to_float(g.k[c] >> 16);
+      }
+    } else {
+      const float x0 = __uint_as_float(g.q[0]), x1 = __uint_as_float(g.q[1]);
+      qT[(2 * lpart) * kQStride + qpos(lr)] = make_float2(x0, x0);
+      qT[(2 * lpart + 1) * kQStride + qpos(lr)] = make_float2(x1, x1);
+#pragma unroll
+      for (int c = 0; c < kBK; ++c) kT[c * kBN + tid] = __uint_as_float(g.k[c]);
+    }
+  };
+
+  // acc[r][cp]: rows rb + r, sub-key pair (cb + 2cp, cb + 2cp + 1), packed.
+  uint64_t acc[8][2];
+  TileRegs<BF16> g;
+  if (ntiles > 0) fetch(0, g);
+  for (int it = 0; it < ntiles; ++it) {
+    const int j0 = (it / nd) * kBN;
+    if (it % nd == 0) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) acc[r][0] = acc[r][1] = 0ull;
+    }
+    __syncthreads();            // every warp is done with the previous tile
+    put(g);
+    __syncthreads();
+    if (it + 1 < ntiles) fetch(it + 1, g);   // in flight during the FMAs below
+#pragma unroll
+    for (int dd = 0; dd < kBK; ++dd) {
+      uint64_t qv[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 q2 = *reinterpret_cast<const float4*>(qT + dd * kQStride + qpos(rb) + 2 * u);
+        qv[2 * u] = f32x2_pack(q2.x, q2.y);
+        qv[2 * u + 1] = f32x2_pack(q2.z, q2.w);
+      }
+      const float4 kk = *reinterpret_cast<const float4*>(kT + dd * kBN + cb);
+      const uint64_t kv[2] = {f32x2_pack(kk.x, kk.y), f32x2_pack(kk.z, kk.w)};
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int cp = 0; cp < 2; ++cp) {
+          if (KIND == SDM_SCORE_DOT) {
+            acc[r][cp] = f32x2_fma(qv[r], kv[cp], acc[r][cp]);
+          } else {
+            const uint64_t df = f32x2_sub(qv[r], kv[cp]);
+            acc[r][cp] = f32x2_fma(df, df, acc[r][cp]);
+          }
+        }
+    }
+    if (it % nd != nd - 1) continue;
+    // Epilogue of sub-key chunk j0.
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const int row = rb + r;
+      const float2 a01 = f32x2_unpack(acc[r][0]), a23 = f32x2_unpack(acc[r][1]);
+      const float av[4] = {a01.x, a01.y, a23.x, a23.y};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int col = j0 + cb + c;
         if (col >= d.s) continue;
-        const float val = (KIND == SDM_SCORE_DOT) ? acc[r][c] : -logf(d.eps + acc[r][c]);
+        const float val = (KIND == SDM_SCORE_DOT) ? av[c] : -logf(d.eps + av[c]);
         if (MODE == kAddrScoresOnly) {
           int sg;
           long long item;
@@ -215,8 +284,9 @@ template <int MODE, bool BF16, int KIND>
 __global__ void __launch_bounds__(kThreads) address_kernel(const AddrArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   const Dims& d = A.d;
-  const SmemLayout L = smem_layout(d.s);
-  float* qT = reinterpret_cast<float*>(smem + L.qT);
+  const SmemLayout L = smem_layout(d.s, list_len(d));
+  const int kst = L.kst;
+  float2* qT = reinterpret_cast<float2*>(smem + L.qT);
   float* kT = reinterpret_cast<float*>(smem + L.kT);
   float* sc = reinterpret_cast<float*>(smem + L.sc);
   float* lv = reinterpret_cast<float*>(smem + L.lv);
@@ -270,8 +340,8 @@ __global__ void __launch_bounds__(kThreads) address_kernel(const AddrArgs A) {
       const int k = sg == 0 ? d.kw : d.kr;
       RowSrc src{sc + (size_t)r * d.s};
       warp_topk<16>(src, d.s, k, ws, lane);
-      float* ov = lv + (r * 2 + p) * kMaxSel;
-      uint32_t* oi = lid + (r * 2 + p) * kMaxSel;
+      float* ov = lv + (r * 2 + p) * kst;
+      uint32_t* oi = lid + (r * 2 + p) * kst;
       for (int e = lane; e < k; e += 32) {
         ov[e] = ws.out_v[e];
         oi[e] = ws.out_id[e];
@@ -288,8 +358,8 @@ __global__ void __launch_bounds__(kThreads) address_kernel(const AddrArgs A) {
     if (item >= BT) continue;
     const int k = sg == 0 ? d.kw : d.kr;
     const int nsel = sg == 0 ? d.W : d.R;
-    warp_merge(lv + (r * 2 + 0) * kMaxSel, lid + (r * 2 + 0) * kMaxSel,
-               lv + (r * 2 + 1) * kMaxSel, lid + (r * 2 + 1) * kMaxSel, k, nsel,
+    warp_merge(lv + (r * 2 + 0) * kst, lid + (r * 2 + 0) * kst,
+               lv + (r * 2 + 1) * kst, lid + (r * 2 + 1) * kst, k, nsel,
                (uint32_t)d.s, stair + sg * kStairMax, nst[sg], ws, lane);
     const long long b = item / d.T, t = item - b * d.T;
     const long long th = (b * d.H + h) * d.T + t;
@@ -302,7 +372,7 @@ __global__ void __launch_bounds__(kThreads) address_kernel(const AddrArgs A) {
 
 template <int MODE, bool BF16, int KIND>
 cudaError_t launch_t(const AddrArgs& A, cudaStream_t stream) {
-  const SmemLayout L = smem_layout(A.d.s);
+  const SmemLayout L = smem_layout(A.d.s, list_len(A.d));
   auto kfn = address_kernel<MODE, BF16, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)L.total);

@@ -154,7 +154,7 @@ def test_address_end_to_end(name):
     oracle_weights(sh_o, S_w, S_r, iw, ir, ww, wr)
 
 
-ROW_SHAPES = [  # bf16 dot scores: the one-thread-per-row kernel
+ROW_SHAPES = [  # bf16 dot scores, s <= 256, d_h <= 64: the tensor-core kernel
     dict(n_sub=32, d_h=16, W=8, R=8, T=90),
     dict(n_sub=40, d_h=32, W=5, R=3, k_w=12, k_r=2, T=70),    # s % 16 != 0, W % 4 != 0
     dict(n_sub=200, d_h=64, W=64, R=16, T=130),
@@ -182,6 +182,35 @@ def test_address_row_kernel_shapes(ov):
     x = generate(w)
     sh_g, sh_o = gshape(w, sdm), oshape(w)
     g = {k: t.to(DEV) for k, t in x.items()}
+    iw, ww, ir, wr = sdm.sdm_address(sh_g, g["q_w"], g["q_r"], g["K"])
+    status_ok()
+    address_checks(w, x, sh_g, sh_o, *(t.cpu().numpy() for t in (iw, ww, ir, wr)), g)
+
+
+FFMA_SHAPES = [  # shapes the tensor-core kernel does not take: the fp32 FFMA contraction
+    dict(n_sub=300, d_h=32, W=64, R=16, bf16=True),                 # s > 256: partial 2nd chunk
+    dict(n_sub=128, d_h=128, W=16, R=64, bf16=True),                # d_h > 64
+    dict(n_sub=64, d_h=32, W=8, R=12, bf16=True, score_kind=1),     # bf16 inverse distance
+    dict(n_sub=400, d_h=16, W=8, R=8, bf16=False),                  # fp32, partial 2nd chunk
+    dict(n_sub=512, d_h=256, W=64, R=8, bf16=False, score_kind=1),  # k = 64 lists at s = 512
+]
+
+
+@pytest.mark.parametrize("ov", FFMA_SHAPES,
+                         ids=lambda o: "s{n_sub}_dh{d_h}_{}".format(
+                             "idw" if o.get("score_kind") else "dot", **o))
+def test_address_ffma_kernel_shapes(ov):
+    ov = dict(ov)
+    if ov.get("score_kind"):
+        ov["qk_std"] = 1.0
+    w = WORKLOADS["mid"].with_(B=1, H=2, T=45, d_v=16, **ov)
+    x = generate(w)
+    sh_g, sh_o = gshape(w, sdm), oshape(w)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    # Sub-scores against the oracle's (fp32 contraction in another order).
+    S = np32(sdm.sdm_subscores(sh_g, g["q_r"], g["K"]))
+    ref = O.subscores(sh_o, np32(x["q_r"]), np32(x["K"]))
+    assert np.max(np.abs(S - ref)) < 1e-5 * max(1.0, float(np.max(np.abs(ref))))
     iw, ww, ir, wr = sdm.sdm_address(sh_g, g["q_w"], g["q_r"], g["K"])
     status_ok()
     address_checks(w, x, sh_g, sh_o, *(t.cpu().numpy() for t in (iw, ww, ir, wr)), g)

@@ -262,6 +262,26 @@ sdm_status sdm_set_scan_tuning(int depth, int col_slice);
  * Shows on a real device that a wait that runs out ends the kernel cleanly. */
 sdm_status sdm_selftest_wait_timeout(long long timeout_ns, void* stream);
 
+/* Measurement reference, not part of the method: the scan's row traffic
+ * ([SDM notes] 2.4: per step of every (chain, column slice) unit, the W + R
+ * rows it touches are fetched and the W written rows stored back) with no
+ * arithmetic and no dependency between steps.  For each of chains x
+ * (d_v / col_slice) units and each of T steps, `loads` row pieces of
+ * col_slice floats are copied from rows drawn uniformly from the unit's chain
+ * in `src` into shared memory, and the first `stores` of them are written to
+ * other uniformly drawn rows of the same chain and columns in `dst`; draws
+ * are a fixed hash of (seed, unit, step, position).  Bytes moved:
+ * chains * d_v * T * (loads + stores) * 4.  A timed call gives the rate HBM
+ * sustains for the scan's access pattern.
+ *   src, dst   device [chains, rows, d_v] float32 (may be the same array; the
+ *              contents of dst afterwards are unspecified); 16-byte aligned.
+ *   col_slice  16, 32 or 64, dividing d_v;  1 <= loads <= 128;
+ *   0 <= stores <= loads;  1 <= rows < 2^32.
+ * Argument errors return SDM_ERR_INVALID_ARG before anything is enqueued. */
+sdm_status sdm_measure_row_traffic(const float* src, float* dst, long long chains,
+                                   long long rows, int d_v, int col_slice, int T, int loads,
+                                   int stores, unsigned seed, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,7 @@ EXPORTS = ["sdm_status_string", "sdm_subscores", "sdm_select", "sdm_address",
            "sdm_undo_workspace_size", "sdm_scan_undo", "sdm_rmsnorm_gate", "sdm_decode",
            "sdm_forward",
            "sdm_get_device_status",
-           "sdm_set_scan_tuning", "sdm_selftest_wait_timeout"]
+           "sdm_set_scan_tuning", "sdm_selftest_wait_timeout", "sdm_measure_row_traffic"]
 
 
 class SdmUnavailable(RuntimeError):
@@ -103,6 +103,8 @@ def lib():
         "sdm_get_device_status": ([P], I),
         "sdm_set_scan_tuning": ([I, I], I),
         "sdm_selftest_wait_timeout": ([ctypes.c_longlong, P], I),
+        "sdm_measure_row_traffic": ([P, P, ctypes.c_longlong, ctypes.c_longlong, I, I, I, I, I,
+                                     ctypes.c_uint, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -386,3 +388,19 @@ def sdm_set_scan_tuning(depth: int = 0, col_slice: int = 0):
 def sdm_selftest_wait_timeout(timeout_ns: int, stream=None):
     _ok(lib().sdm_selftest_wait_timeout(int(timeout_ns), _stream(stream)),
         "sdm_selftest_wait_timeout")
+
+
+def sdm_measure_row_traffic(src, dst, col_slice: int, T: int, loads: int, stores: int,
+                            seed: int = 1, stream=None) -> int:
+    """Measurement reference: the scan's row traffic without its arithmetic
+    on tables src, dst [chains, rows, d_v] float32; returns the bytes moved."""
+    chains, rows, dv = src.shape
+    if tuple(dst.shape) != (chains, rows, dv):
+        raise ValueError("src and dst shapes differ")
+    f32 = (torch.float32,)
+    _ok(lib().sdm_measure_row_traffic(_ptr(src, "src", f32, src.numel()),
+                                      _ptr(dst, "dst", f32, src.numel()), chains, rows, dv,
+                                      col_slice, T, loads, stores, seed & 0xffffffff,
+                                      _stream(stream)),
+        "sdm_measure_row_traffic")
+    return chains * dv * T * (loads + stores) * 4

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libsdm_gb300.so")
 SOURCES = ["sdm_api.cu", "address.cu", "plan.cu", "scan.cu", "undo.cu", "epilogue.cu",
-           "decode.cu", "sdm_noalloc.cu"]
+           "decode.cu", "sdm_noalloc.cu", "rowtraffic.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -66,6 +66,11 @@ cudaError_t launch_rmsnorm_gate(const Dims& d, const float* y, const void* g, co
 
 // Fused decode (decode.cu): one CTA per (b,h) chain runs its T steps --
 // addressing, write, read and, when out is non-null, the epilogue.
+// rowtraffic.cu: random row pieces in the scan's unit layout, no arithmetic.
+cudaError_t launch_row_traffic(const float* src, float* dst, long long chains, long long rows,
+                               int dv, int col_slice, int T, int loads, int stores,
+                               uint32_t seed, cudaStream_t stream);
+
 cudaError_t launch_decode(const Dims& d, const void* q_w, const void* q_r, const void* K,
                           const void* alpha, const void* beta, const void* v, float* M, float* y,
                           int32_t* idx_w, float* wt_w, int32_t* idx_r, float* wt_r,

@@ -389,4 +389,19 @@ sdm_status sdm_selftest_wait_timeout(long long timeout_ns, void* stream) {
   return from_cuda(cudaGetLastError());
 }
 
+sdm_status sdm_measure_row_traffic(const float* src, float* dst, long long chains,
+                                   long long rows, int d_v, int col_slice, int T, int loads,
+                                   int stores, unsigned seed, void* stream) {
+  if (chains < 0 || rows < 1 || rows > 0xffffffffll || T < 0) return SDM_ERR_INVALID_ARG;
+  if (col_slice != 16 && col_slice != 32 && col_slice != 64) return SDM_ERR_INVALID_ARG;
+  if (d_v < col_slice || d_v % col_slice != 0) return SDM_ERR_INVALID_ARG;
+  if (loads < 1 || loads > 128 || stores < 0 || stores > loads) return SDM_ERR_INVALID_ARG;
+  if (chains * (d_v / col_slice) > 0x7fffffffll) return SDM_ERR_UNSUPPORTED;
+  if (chains == 0 || T == 0) return SDM_OK;   // no work: pointers are not looked at
+  SDM_CHECK_PTR(src);
+  SDM_CHECK_PTR(dst);
+  return from_cuda(launch_row_traffic(src, dst, chains, rows, d_v, col_slice, T, loads, stores,
+                                      seed, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

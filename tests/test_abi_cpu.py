@@ -189,3 +189,22 @@ def test_decode_arguments(L):
     # No work: returns before looking at the pointers (NULL is fine).
     for kw in (dict(T=0), dict(B=0), dict(H=0)):
         assert dec([None] * 12, shape=good_shape(**kw)) == 0
+
+
+def test_measure_row_traffic_arguments(L):
+    rc = L.sdm_measure_row_traffic
+    good = (FAKE, FAKE, 4, 1024, 128, 32, 8, 128, 64, 1, None)
+    # Each bad argument is refused before any CUDA call.
+    bad = {2: -1, 3: 0, 4: 40, 5: 48, 6: -1, 7: 0, 8: -1}
+    for i, val in bad.items():
+        a = list(good)
+        a[i] = val
+        assert rc(*a) == 1, (i, val)
+    for loads, stores in ((129, 0), (8, 9), (0, 0)):
+        assert rc(FAKE, FAKE, 4, 1024, 128, 32, 8, loads, stores, 1, None) == 1
+    assert rc(None, FAKE, 4, 1024, 128, 32, 8, 128, 64, 1, None) == 1
+    assert rc(FAKE, MISALIGNED, 4, 1024, 128, 32, 8, 128, 64, 1, None) == 1
+    assert rc(FAKE, FAKE, 4, 1 << 32, 128, 32, 8, 128, 64, 1, None) == 1     # rows >= 2^32
+    # No work: nothing is launched and the pointers are not looked at.
+    assert rc(None, None, 0, 1024, 128, 32, 8, 128, 64, 1, None) == 0
+    assert rc(None, None, 4, 1024, 128, 32, 0, 128, 64, 1, None) == 0

@@ -59,7 +59,7 @@ constexpr int kThreads = kConsumers + 32 + kLoaders;
 template <int MINB>
 __host__ __device__ constexpr int prefetch_steps() { return MINB == 1 ? 16 : 4; }
 constexpr int kPrefetchBatch = 4;   // steps the producer handles per loop pass
-constexpr int kSlack = 4;        // steps the producer may prepare beyond the need
+constexpr int kSlack = 2;        // steps the producer may prepare beyond the need
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 
 // One step's metadata.  Every array starts on a 16-byte boundary (16-byte
@@ -97,16 +97,20 @@ struct ScanLayout {
   int NS, MR;
 };
 
-__host__ __device__ inline ScanLayout scan_layout(int CW, int W, int R, int D, int kP) {
+__host__ __device__ inline ScanLayout scan_layout(int CW, int W, int R, int D, int kP,
+                                                  bool fig2) {
   ScanLayout L;
-  L.NS = 2 * D;
+  // Write tiles live from the oldest step a consumer may forward from
+  // (t - D + 1) to the newest a loader may be filling (t + D - 1).
+  L.NS = 2 * D - 1;
   L.MR = D + kP + kPrefetchBatch + kSlack;
   size_t o = 0;
   L.meta = o;  o += sizeof(MetaSlot) * L.MR;
   L.wtile = o; o += sizeof(float) * (size_t)L.NS * W * CW;
   L.rtile = o; o += sizeof(float) * (size_t)D * R * CW;
   L.ypart = o; o += sizeof(float) * 2 * 8 * CW;
-  L.vpart = o; o += sizeof(float) * 8 * CW;      // per-warp partials of vhat (Fig. 2 form)
+  L.vpart = o;                                    // per-warp partials of vhat (Fig. 2 form)
+  if (fig2) o += sizeof(float) * 8 * CW;
   L.bars = o;  o += sizeof(uint64_t) * (2 * L.MR + D);
   L.total = o;
   return L;
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, MINB) scan_kernel(const ScanArgs A) 
   const Dims& d = A.d;
   const int D = A.depth;
   const int W = d.W, R = d.R, T = d.T, dv = d.dv;
-  const ScanLayout L = scan_layout(CW, W, R, D, prefetch_steps<MINB>());
+  const ScanLayout L = scan_layout(CW, W, R, D, prefetch_steps<MINB>(), FIG2);
   const int NS = L.NS, MR = L.MR;
   const int nslice = dv / CW;
   const int chain = blockIdx.x / nslice;
@@ -920,7 +924,7 @@ template <int CW, bool BF16>
 cudaError_t launch_t(const ScanArgs& A, bool one_per_sm, cudaStream_t stream) {
   const bool fig2 = A.d.update == SDM_UPDATE_SHARED_RESIDUAL, logged = A.undo != nullptr;
   const int kp = one_per_sm && !fig2 && !logged ? prefetch_steps<1>() : prefetch_steps<2>();
-  const size_t smem = scan_layout(CW, A.d.W, A.d.R, A.depth, kp).total;
+  const size_t smem = scan_layout(CW, A.d.W, A.d.R, A.depth, kp, fig2).total;
   auto kfn = fig2 ? (logged ? scan_kernel<CW, BF16, true, true, 2> : scan_kernel<CW, BF16, true, false, 2>)
                   : (logged ? scan_kernel<CW, BF16, false, true, 2>
                             : (one_per_sm ? scan_kernel<CW, BF16, false, false, 1>
@@ -958,8 +962,8 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   const long long per_sm = (units + sms - 1) / sms;
   // The build that runs (see launch_t) and its metadata prefetch distance.
   const bool one = per_sm <= 1;
-  const int kp = one && d.update != SDM_UPDATE_SHARED_RESIDUAL && !undo ? prefetch_steps<1>()
-                                                                        : prefetch_steps<2>();
+  const bool fig2 = d.update == SDM_UPDATE_SHARED_RESIDUAL;
+  const int kp = one && !fig2 && !undo ? prefetch_steps<1>() : prefetch_steps<2>();
   const size_t budget = per_sm <= 1    ? lim.smem_per_cta
                         : per_sm == 2 ? lim.smem_per_sm / 2 - 1024
                                       : lim.smem_per_sm / 3 - 1024;
@@ -967,11 +971,11 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   if (D == 0) {
     D = 1;
     for (int cand = 2; cand <= 16; ++cand)
-      if (scan_layout(cw, d.W, d.R, cand, kp).total <= budget) D = cand;
+      if (scan_layout(cw, d.W, d.R, cand, kp, fig2).total <= budget) D = cand;
   }
   if (D < 1 || D > 16) return cudaErrorInvalidValue;
   // A requested depth is a hint: shrink it until the ring fits on chip.
-  while (D > 1 && scan_layout(cw, d.W, d.R, D, kp).total > lim.smem_per_cta) --D;
+  while (D > 1 && scan_layout(cw, d.W, d.R, D, kp, fig2).total > lim.smem_per_cta) --D;
 
   int16_t* codes = static_cast<int16_t*>(workspace);
   cudaError_t e = launch_plan(d, idx_w, idx_r, codes, D, status, stream);

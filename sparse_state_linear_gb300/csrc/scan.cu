@@ -49,8 +49,12 @@ namespace sdm {
 namespace {
 
 constexpr int kConsumers = 256;
-constexpr int kLoaders = 128;    // loader threads (4 warps) that fetch the rows
-constexpr int kThreads = kConsumers + 32 + kLoaders;
+// Loader threads that fetch the rows: 4 warps where two CTAs share an SM
+// (issue slots are scarce there), 6 where a unit has the SM to itself.
+template <int MINB>
+__host__ __device__ constexpr int loader_threads() { return MINB == 1 ? 192 : 128; }
+template <int MINB>
+__host__ __device__ constexpr int scan_threads() { return kConsumers + 32 + loader_threads<MINB>(); }
 // Producer's metadata prefetch distance (steps): the copies of a step are
 // waited for kP steps after they were issued, so at most kP steps' metadata
 // is in flight; their latency (microseconds under load) over kP bounds the
@@ -143,7 +147,8 @@ struct Ring {
 // workloads; 1 where every unit has an SM of its own and the per-step
 // latency decides, which leaves the compiler twice the registers).
 template <int CW, bool BF16, bool FIG2, bool UNDO, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB) scan_kernel(const ScanArgs A) {
+__global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const ScanArgs A) {
+  constexpr int kLoaders = loader_threads<MINB>();
   constexpr int CH = CW / 4;               // 16-byte chunks per row slice
   constexpr int RP = kConsumers / CH;      // rows per consumer pass
   constexpr int IB = BF16 ? 2 : 4;         // input element bytes
@@ -629,9 +634,28 @@ __global__ void __launch_bounds__(kThreads, MINB) scan_kernel(const ScanArgs A) 
       return reinterpret_cast<const float4*>(wt0 + sl * wslot + (code & 63) * rowb);
     };
     for (int t = 0; t < T; ++t) {
-      // Rows and metadata of step t: every lane tests both barriers, the
-      // previous step's read sum is reduced meanwhile.
-      {
+      // Rows and metadata of step t; the previous step's read sum is reduced
+      // meanwhile.
+      if constexpr (MINB == 2) {
+        // Two CTAs share the SM and issue slots are the limit: one warp
+        // tests the barriers, the other consumer warps sleep in a hardware
+        // barrier meanwhile (which also orders their reads after its acquire).
+        if (t > 0) store_partial(t - 1, acc_prev);
+        bool bad = false;
+        if (warp == 0) {
+          const bool r0 = mbar_test_wait(&rfull[ri], rph);
+          const bool m0 = mbar_test_wait(&mfull[mi], mph);
+          if (!__all_sync(0xffffffffu, r0 && m0)) {
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait2_bounded(&rfull[ri], rph, &mfull[mi], mph, kTimeoutNs);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+              if (lane == 0) record_status(A.status, SDM_ERR_TIMEOUT);
+              bad = true;
+            }
+          }
+        }
+        if (named_bar_or(4, kConsumers, bad)) aborted = true;
+      } else {
         const bool r0 = mbar_test_wait(&rfull[ri], rph);
         const bool m0 = mbar_test_wait(&mfull[mi], mph);
         if (t > 0) store_partial(t - 1, acc_prev);
@@ -934,7 +958,8 @@ cudaError_t launch_t(const ScanArgs& A, bool one_per_sm, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const long long units = (long long)A.d.B * A.d.H * (A.d.dv / CW);
   if (units == 0 || A.d.T == 0) return cudaSuccess;
-  kfn<<<(unsigned)units, kThreads, smem, stream>>>(A);
+  const bool one = !fig2 && !logged && one_per_sm;     // the MINB = 1 build
+  kfn<<<(unsigned)units, one ? scan_threads<1>() : scan_threads<2>(), smem, stream>>>(A);
   return cudaGetLastError();
 }
 

@@ -143,7 +143,7 @@ __device__ void score_half(const AddrArgs& A, int p, float2* qT, float* kT, floa
   size_t qoff = 0;
   if (lvalid) {
     const long long b = litem / d.T, t = litem - b * d.T;
-    const long long th = (b * d.H + h) * d.T + t;
+    const long long th = (b * d.H + h) * d.Ts + t;
     qoff = (size_t)(th * 2 + p) * d.dh;
   }
   const void* qbase = (lsig == 0) ? A.q0 : A.q1;
@@ -269,7 +269,7 @@ __device__ void score_half(const AddrArgs& A, int p, float2* qT, float* kT, floa
           row_item<MODE>(row, sg, item);
           if (item < BT) {
             const long long b = item / d.T, t = item - b * d.T;
-            const long long th = (b * d.H + h) * d.T + t;
+            const long long th = (b * d.H + h) * d.Ts + t;
             A.S[(size_t)(th * 2 + p) * d.s + col] = val;
           }
         } else {
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kThreads) address_kernel(const AddrArgs A) {
         float val = 0.f;
         if (item < BT) {
           const long long b = item / d.T, t = item - b * d.T;
-          const long long th = (b * d.H + h) * d.T + t;
+          const long long th = (b * d.H + h) * d.Ts + t;
           const float* f = sg == 0 ? A.f0 : A.f1;
           val = __ldg(f + (size_t)(th * 2 + p) * d.s + j);
         }
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kThreads) address_kernel(const AddrArgs A) {
                lv + (r * 2 + 1) * kst, lid + (r * 2 + 1) * kst, k, nsel,
                (uint32_t)d.s, stair + sg * kStairMax, nst[sg], ws, lane);
     const long long b = item / d.T, t = item - b * d.T;
-    const long long th = (b * d.H + h) * d.T + t;
+    const long long th = (b * d.H + h) * d.Ts + t;
     int32_t* io = (sg == 0 ? A.idx_w : A.idx_r) + (size_t)th * nsel;
     float* wo = (sg == 0 ? A.wt_w : A.wt_r) + (size_t)th * nsel;
     warp_softmax_store(ws, nsel, io, wo, lane);
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) address_tc_kernel(const AddrArg
     long long th = -1;
     if (item < BT) {
       const long long b = item / d.T, t = item - b * d.T;
-      th = (b * d.H + h) * d.T + t;
+      th = (b * d.H + h) * d.Ts + t;
     }
     rth[tid] = th;
   } else if (tid < kTcRows + 2 * kMaxSel) {
@@ -640,6 +640,8 @@ cudaError_t launch_mode(const AddrArgs& A, cudaStream_t stream) {
 }
 
 }  // namespace
+
+bool address_on_tensor_cores(const Dims& d) { return tc_eligible(d); }
 
 cudaError_t launch_address(int mode, const Dims& d, const void* q0, const void* q1,
                            const void* K, const float* f0, const float* f1,

@@ -12,6 +12,8 @@ namespace sdm {
 // Resolved per-call parameters (validated by the API layer).
 struct Dims {
   int B, H, T, s, dh, dv, W, R, kw, kr;
+  int Ts;        // rows between chains in the [B, H, T, ...] layouts: T, or the
+                 // full length when a call covers a window of steps
   int in_dtype;  // SDM_F32 / SDM_BF16
   int score;     // SDM_SCORE_DOT / SDM_SCORE_IDW
   float eps;
@@ -28,6 +30,8 @@ enum AddrMode { kAddrFused = 0, kAddrSelectOnly = 1, kAddrScoresOnly = 2 };
 //  kAddrFused:      q0 = q_w, q1 = q_r -> idx/wt of both branches.
 //  kAddrSelectOnly: f0 = sub_w, f1 = sub_r (float32 sub-scores) -> idx/wt.
 //  kAddrScoresOnly: q0 = the branch's half-queries -> S (float32).
+// Whether the fused addressing of this shape runs on the tensor cores.
+bool address_on_tensor_cores(const Dims& d);
 cudaError_t launch_address(int mode, const Dims& d, const void* q0, const void* q1,
                            const void* K, const float* f0, const float* f1,
                            int32_t* idx_w, float* wt_w, int32_t* idx_r, float* wt_r,
@@ -66,6 +70,31 @@ cudaError_t launch_rmsnorm_gate(const Dims& d, const float* y, const void* g, co
 
 // Fused decode (decode.cu): one CTA per (b,h) chain runs its T steps --
 // addressing, write, read and, when out is non-null, the epilogue.
+// sdm_api.cu: the overlapped forward (addressing of window k+1 beside the
+// scan of window k).  forward_segments gives the number of windows (1 = none);
+// run_segmented_forward returns a cudaError_t, or -1 if its streams could not
+// be set up (nothing enqueued).
+struct SegmentedForward {
+  Dims d;
+  const char* q_w;
+  const char* q_r;
+  const void* K;
+  const char* alpha;
+  const char* beta;
+  const char* v;
+  float* M;
+  float* y;
+  int32_t* idx_w;
+  float* wt_w;
+  int32_t* idx_r;
+  float* wt_r;
+  int16_t* codes;
+  int in_bytes, depth, col_slice;
+  unsigned* status;
+};
+int forward_segments(const Dims& d);
+int run_segmented_forward(const SegmentedForward& f, int S, cudaStream_t caller);
+
 // rowtraffic.cu: random row pieces in the scan's unit layout, no arithmetic.
 cudaError_t launch_row_traffic(const float* src, float* dst, long long chains, long long rows,
                                int dv, int col_slice, int T, int loads, int stores,

@@ -34,6 +34,7 @@ struct PlanArgs {
   const int32_t* idx_r;
   int16_t* codes;
   int T, W, R, depth;
+  int Ts;              // rows between chains in the index / code layouts
   uint32_t N;
   unsigned* status;
 };
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(kPlanThreads, 2) plan_kernel(const PlanArgs P)
   const int t1 = min(P.T, t0 + kPlanTB);
   const int s0 = max(0, t0 - (P.depth - 1));
   const int W = P.W, R = P.R, WR = W + R, CP = code_pitch(W, R);
-  const size_t base = (size_t)chain * P.T;
+  const size_t base = (size_t)chain * P.Ts;
   if constexpr (VEC) {
     constexpr int kWarps = kPlanThreads / 32;
     constexpr int kLook = kPlanTB / kWarps;                        // steps per warp
@@ -247,7 +248,7 @@ cudaError_t launch_plan(const Dims& d, const int32_t* idx_w, const int32_t* idx_
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPlanSmem);
   if (e != cudaSuccess) return e;
-  PlanArgs P{idx_w, idx_r, codes, d.T, d.W, d.R, depth, (uint32_t)d.N(), status};
+  PlanArgs P{idx_w, idx_r, codes, d.T, d.W, d.R, depth, d.Ts, (uint32_t)d.N(), status};
   dim3 grid((unsigned)((d.T + kPlanTB - 1) / kPlanTB), (unsigned)chains);
   kern<<<grid, kPlanThreads, kPlanSmem, stream>>>(P);
   return cudaGetLastError();

@@ -121,6 +121,9 @@ __host__ __device__ inline ScanLayout scan_layout(int CW, int W, int R, int D, i
 }
 
 
+// Bytes between the shared-memory partitions of the units of one CTA.
+__host__ __device__ inline size_t unit_smem_stride(size_t total) { return (total + 127) & ~(size_t)127; }
+
 template <bool BF16>
 __device__ __forceinline__ float4 load_v4(const unsigned char* vraw, int c) {
   if (BF16) {
@@ -143,11 +146,16 @@ struct Ring {
   }
 };
 
-// MINB: CTAs per SM the launch is sized for (2 on the bandwidth-bound
+// MINB: units per SM the build is sized for (2 on the bandwidth-bound
 // workloads; 1 where every unit has an SM of its own and the per-step
 // latency decides, which leaves the compiler twice the registers).
-template <int CW, bool BF16, bool FIG2, bool UNDO, int MINB>
-__global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const ScanArgs A) {
+// PAIR: units per CTA.  With PAIR = 2 a CTA runs two independent units side
+// by side (each with its own warps, shared-memory partition and named
+// barriers), so a launch of U units occupies exactly U / 2 SMs and leaves
+// the others free for concurrent work (the addressing of the next segment).
+template <int CW, bool BF16, bool FIG2, bool UNDO, int MINB, int PAIR>
+__global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : MINB)
+    scan_kernel(const ScanArgs A) {
   constexpr int kLoaders = loader_threads<MINB>();
   constexpr int CH = CW / 4;               // 16-byte chunks per row slice
   constexpr int RP = kConsumers / CH;      // rows per consumer pass
@@ -157,7 +165,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
   // reductions; tile row k keeps its chunk c at 16-byte position c ^ (k & 7)
   // (conflict-free when the lanes of a warp walk the rows of one chunk).
   constexpr bool COL = FIG2 && CW == 32;
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_all[];
 
   const Dims& d = A.d;
   const int D = A.depth;
@@ -165,9 +173,14 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
   const ScanLayout L = scan_layout(CW, W, R, D, prefetch_steps<MINB>(), FIG2);
   const int NS = L.NS, MR = L.MR;
   const int nslice = dv / CW;
-  const int chain = blockIdx.x / nslice;
-  const int c0 = (blockIdx.x - chain * nslice) * CW;
-  const size_t th0 = (size_t)chain * T;    // flat (b,h,t=0) row
+  // This unit: its threads, shared-memory partition and named barriers.
+  const int sub = PAIR == 1 ? 0 : (int)(threadIdx.x / scan_threads<MINB>());
+  const long long unit = (long long)blockIdx.x * PAIR + sub;
+  unsigned char* const smem = smem_all + (size_t)sub * unit_smem_stride(L.total);
+  const int bb = 4 * sub;                  // named barriers bb + 1 .. bb + 4
+  const int chain = (int)(unit / nslice);
+  const int c0 = (int)(unit - (long long)chain * nslice) * CW;
+  const size_t th0 = (size_t)chain * d.Ts;  // flat (b,h,t=0) row
   float* Mc = A.M + (size_t)chain * (size_t)d.N() * dv + c0;
   const int CP = code_pitch(W, R);
 
@@ -180,7 +193,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
   const uint32_t wslot = (uint32_t)(W * CW * 4), rslot = (uint32_t)(R * CW * 4);
   constexpr uint32_t rowb = (uint32_t)(CW * 4);
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x - sub * scan_threads<MINB>(), lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     for (int i = 0; i < MR; ++i) {
       mbar_init(&mfull[i], 32);
@@ -189,6 +202,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
     for (int i = 0; i < D; ++i) mbar_init(&rfull[i], kLoaders);
   }
   __syncthreads();
+  if (unit >= (long long)d.B * d.H * nslice) return;   // odd unit count: idle half
 
   if (warp == kConsumers / 32) {
     // ------------------------------------------------------------ producer
@@ -372,7 +386,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
         if (!ok) record_status(A.status, SDM_ERR_TIMEOUT);
         failed = !ok;
       }
-      if (named_bar_or(3, kLoaders, failed)) break;
+      if (named_bar_or(bb + 3, kLoaders, failed)) break;
       const MetaSlot* m = meta + mu.i;
       // Only rows whose current value is in HBM (code -1) are fetched; a
       // forwarded (>= 0) or invalid (-2) row is not.
@@ -495,7 +509,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
         }
       }
       // The one block barrier of a step (a timeout becomes a uniform exit).
-      if (named_bar_or(1, kConsumers, aborted)) {
+      if (named_bar_or(bb + 1, kConsumers, aborted)) {
         aborted = true;
         break;
       }
@@ -654,7 +668,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
             }
           }
         }
-        if (named_bar_or(4, kConsumers, bad)) aborted = true;
+        if (named_bar_or(bb + 4, kConsumers, bad)) aborted = true;
       } else {
         const bool r0 = mbar_test_wait(&rfull[ri], rph);
         const bool m0 = mbar_test_wait(&mfull[mi], mph);
@@ -710,7 +724,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
       }
       // The one block barrier of a step; it also turns a timeout anywhere
       // into a decision every consumer takes at the same point.
-      if (named_bar_or(1, kConsumers, aborted)) {
+      if (named_bar_or(bb + 1, kConsumers, aborted)) {
         aborted = true;
         break;
       }
@@ -766,7 +780,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
       if constexpr (UNDO) undo_p += undo_step;
     }
     if (T > 0) store_partial(T - 1, acc_prev);
-    named_bar_sync(1, kConsumers);
+    named_bar_sync(bb + 1, kConsumers);
     if (!aborted && T > 0 && warp == ((T - 1) & 7)) finalize(T - 1);
     return;
   }
@@ -865,7 +879,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
       }
       // Every consumer reaches this barrier each step (a timeout becomes a
       // uniform exit here, as at the step barrier below).
-      if (named_bar_or(2, kConsumers, aborted)) {
+      if (named_bar_or(bb + 2, kConsumers, aborted)) {
         aborted = true;
         break;
       }
@@ -899,7 +913,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
     }
     // The one block barrier of a step; it also turns a timeout anywhere
     // into a decision every consumer takes at the same point.
-    if (named_bar_or(1, kConsumers, aborted)) {
+    if (named_bar_or(bb + 1, kConsumers, aborted)) {
       aborted = true;
       break;
     }
@@ -940,26 +954,36 @@ __global__ void __launch_bounds__(scan_threads<MINB>(), MINB) scan_kernel(const 
     rf.next();
   }
   if (T > 0) store_partial(T - 1, acc_prev);
-  named_bar_sync(1, kConsumers);
+  named_bar_sync(bb + 1, kConsumers);
   if (!aborted && T > 0 && warp == ((T - 1) & 7)) finalize(T - 1);
 }
+
+// Pair build (two units per CTA) for the Eq. (4) scan where two units share
+// an SM.
+constexpr bool kPairUnits = true;
 
 template <int CW, bool BF16>
 cudaError_t launch_t(const ScanArgs& A, bool one_per_sm, cudaStream_t stream) {
   const bool fig2 = A.d.update == SDM_UPDATE_SHARED_RESIDUAL, logged = A.undo != nullptr;
-  const int kp = one_per_sm && !fig2 && !logged ? prefetch_steps<1>() : prefetch_steps<2>();
-  const size_t smem = scan_layout(CW, A.d.W, A.d.R, A.depth, kp, fig2).total;
-  auto kfn = fig2 ? (logged ? scan_kernel<CW, BF16, true, true, 2> : scan_kernel<CW, BF16, true, false, 2>)
-                  : (logged ? scan_kernel<CW, BF16, false, true, 2>
-                            : (one_per_sm ? scan_kernel<CW, BF16, false, false, 1>
-                                          : scan_kernel<CW, BF16, false, false, 2>));
+  const bool one = !fig2 && !logged && one_per_sm;      // the MINB = 1 build
+  const bool pair = kPairUnits && !fig2 && !logged && !one_per_sm;
+  const int kp = one ? prefetch_steps<1>() : prefetch_steps<2>();
+  const size_t total = scan_layout(CW, A.d.W, A.d.R, A.depth, kp, fig2).total;
+  const size_t smem = pair ? 2 * unit_smem_stride(total) : total;
+  auto kfn = fig2 ? (logged ? scan_kernel<CW, BF16, true, true, 2, 1>
+                            : scan_kernel<CW, BF16, true, false, 2, 1>)
+                  : (logged ? scan_kernel<CW, BF16, false, true, 2, 1>
+                            : (one ? scan_kernel<CW, BF16, false, false, 1, 1>
+                                   : (pair ? scan_kernel<CW, BF16, false, false, 2, 2>
+                                           : scan_kernel<CW, BF16, false, false, 2, 1>)));
   cudaError_t e =
       cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long units = (long long)A.d.B * A.d.H * (A.d.dv / CW);
   if (units == 0 || A.d.T == 0) return cudaSuccess;
-  const bool one = !fig2 && !logged && one_per_sm;     // the MINB = 1 build
-  kfn<<<(unsigned)units, one ? scan_threads<1>() : scan_threads<2>(), smem, stream>>>(A);
+  const long long grid = pair ? (units + 1) / 2 : units;
+  const int threads = one ? scan_threads<1>() : (pair ? 2 : 1) * scan_threads<2>();
+  kfn<<<(unsigned)grid, threads, smem, stream>>>(A);
   return cudaGetLastError();
 }
 
@@ -992,6 +1016,8 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   const size_t budget = per_sm <= 1    ? lim.smem_per_cta
                         : per_sm == 2 ? lim.smem_per_sm / 2 - 1024
                                       : lim.smem_per_sm / 3 - 1024;
+  // (The pair build puts two such partitions, each rounded to 128 bytes, in
+  // one CTA: 2 * (smem_per_sm / 2 - 1024) stays within smem_per_cta.)
   int D = depth;
   if (D == 0) {
     D = 1;

@@ -65,6 +65,7 @@ sdm_status check_shape(const sdm_shape* sh, Dims* d) {
   d->B = sh->B;
   d->H = sh->H;
   d->T = sh->T;
+  d->Ts = sh->T;
   d->s = s;
   d->dh = sh->d_h;
   d->dv = sh->d_v;
@@ -116,6 +117,92 @@ DeviceLimits device_limits() {
     known[dev] = true;
   }
   return cache[dev];
+}
+
+// ----------------------------------------------------------- forward overlap
+// sdm_forward cuts T into S windows of steps.  The addressing of window k+1
+// (which reads only q and K) runs on a low-priority stream while the scan of
+// window k (which carries M from window to window) runs on a high-priority
+// one, so the addressing fills what the scan leaves of the GPU and the scan
+// gets SMs first whenever they free up.  Each window's scan waits for its
+// addressing; both streams are joined back into the caller's stream, so the
+// call keeps one-stream semantics (and can be captured in a graph).  Results
+// are bit-identical to sdm_address followed by sdm_scan: addressing is per
+// token, and a scan of consecutive windows equals one scan.
+
+// Windows: the tensor-core addressing of a window fits beside the scan in the
+// SMs it leaves free, so short windows (512 steps, at most 32 of them) hide
+// most of it; the FFMA addressing is too heavy to hide there, and only the
+// scan's per-window ramps are worth overlapping (4 windows).
+int forward_segments(const Dims& d) {
+  if (d.T < 2048) return 1;
+  const int s = address_on_tensor_cores(d) ? d.T / 512 : 4;
+  return s > 32 ? 32 : s;
+}
+
+namespace {
+struct ForwardStreams {
+  bool ready = false;
+  cudaStream_t hi = nullptr, lo = nullptr;
+  cudaEvent_t start = nullptr, addr = nullptr, hi_end = nullptr, lo_end = nullptr;
+};
+std::mutex g_fwd_mu[64];
+ForwardStreams g_fwd[64];
+}  // namespace
+
+int run_segmented_forward(const SegmentedForward& f, int S, cudaStream_t caller) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  // Enqueueing holds the device's lock: the side streams and events are shared.
+  std::lock_guard<std::mutex> lk(g_fwd_mu[dev]);
+  ForwardStreams& fs = g_fwd[dev];
+  if (!fs.ready) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return -1;
+    if (cudaStreamCreateWithPriority(&fs.hi, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&fs.lo, cudaStreamNonBlocking, least) != cudaSuccess ||
+        cudaEventCreateWithFlags(&fs.start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&fs.addr, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&fs.hi_end, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&fs.lo_end, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return -1;
+    }
+    fs.ready = true;
+  }
+  const Dims& d = f.d;
+  cudaError_t e = cudaEventRecord(fs.start, caller);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(fs.hi, fs.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(fs.lo, fs.start, 0);
+  if (e != cudaSuccess) return (int)e;
+  const int tseg = (d.T + S - 1) / S;
+  const size_t qrow = (size_t)2 * d.dh * f.in_bytes;       // bytes per token of q
+  const size_t CP = (size_t)code_pitch(d.W, d.R);
+  for (int t0 = 0; t0 < d.T && e == cudaSuccess; t0 += tseg) {
+    Dims w = d;
+    w.T = d.T - t0 < tseg ? d.T - t0 : tseg;
+    w.Ts = d.T;
+    e = launch_address(kAddrFused, w, f.q_w + t0 * qrow, f.q_r + t0 * qrow, f.K, nullptr,
+                       nullptr, f.idx_w + (size_t)t0 * d.W, f.wt_w + (size_t)t0 * d.W,
+                       f.idx_r + (size_t)t0 * d.R, f.wt_r + (size_t)t0 * d.R, nullptr,
+                       f.status, fs.lo);
+    if (e == cudaSuccess) e = cudaEventRecord(fs.addr, fs.lo);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(fs.hi, fs.addr, 0);
+    if (e == cudaSuccess)
+      e = launch_scan(w, f.idx_w + (size_t)t0 * d.W, f.wt_w + (size_t)t0 * d.W,
+                      f.idx_r + (size_t)t0 * d.R, f.wt_r + (size_t)t0 * d.R,
+                      f.alpha + (size_t)t0 * f.in_bytes, f.beta + (size_t)t0 * f.in_bytes,
+                      f.v + (size_t)t0 * d.dv * f.in_bytes, f.M, f.y + (size_t)t0 * d.dv,
+                      nullptr, f.codes + (size_t)t0 * CP, f.depth, f.col_slice, f.status,
+                      fs.hi);
+  }
+  // Join both streams back into the caller's, also after a failed launch, so
+  // nothing of this call is left running behind the caller's back.
+  cudaError_t j = cudaEventRecord(fs.hi_end, fs.hi);
+  if (j == cudaSuccess) j = cudaEventRecord(fs.lo_end, fs.lo);
+  if (j == cudaSuccess) j = cudaStreamWaitEvent(caller, fs.hi_end, 0);
+  if (j == cudaSuccess) j = cudaStreamWaitEvent(caller, fs.lo_end, 0);
+  return (int)(e != cudaSuccess ? e : j);
 }
 
 sdm_status api_check_shape(const sdm_shape* shape, Dims* d) { return check_shape(shape, d); }
@@ -296,6 +383,33 @@ sdm_status sdm_forward(const sdm_shape* shape, const void* q_w, const void* q_r,
   SDM_CHECK_PTR(y);
   SDM_CHECK_PTR(workspace);
   if (ws_bytes < scan_workspace_bytes(d)) return SDM_ERR_INVALID_ARG;
+  const int S = forward_segments(d);
+  if (S > 1) {
+    SDM_CHECK_PTR(q_w);
+    SDM_CHECK_PTR(q_r);
+    SDM_CHECK_PTR(K);
+    SDM_CHECK_PTR(idx_w);
+    SDM_CHECK_PTR(wt_w);
+    SDM_CHECK_PTR(idx_r);
+    SDM_CHECK_PTR(wt_r);
+    int depth, cs;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      depth = g_depth;
+      cs = g_colslice;
+    }
+    if (cs && d.dv % cs != 0) return SDM_ERR_INVALID_ARG;
+    unsigned* sp = nullptr;
+    if ((st = status_ptr(&sp)) != SDM_OK) return st;
+    const int ib = d.in_dtype == SDM_BF16 ? 2 : 4;
+    SegmentedForward f{d,     static_cast<const char*>(q_w), static_cast<const char*>(q_r), K,
+                       static_cast<const char*>(alpha), static_cast<const char*>(beta),
+                       static_cast<const char*>(v), M, y, idx_w, wt_w, idx_r, wt_r,
+                       static_cast<int16_t*>(workspace), ib, depth, cs, sp};
+    const int rc = run_segmented_forward(f, S, static_cast<cudaStream_t>(stream));
+    if (rc >= 0) return from_cuda(static_cast<cudaError_t>(rc));
+    // The side streams could not be set up: one stream, unsegmented.
+  }
   st = sdm_address(shape, q_w, q_r, K, idx_w, wt_w, idx_r, wt_r, stream);
   if (st != SDM_OK) return st;
   return sdm_scan(shape, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, workspace, ws_bytes,

@@ -716,3 +716,31 @@ def test_decode_agrees_with_forward():
     ya, yb = np32(a["y"]), np32(b["y"])
     sm = same.cpu().numpy()
     assert max_rel(ya[sm], yb[sm]) <= FTOL
+
+
+SEGMENTED = [  # sdm_forward cuts T >= 2048 into windows and overlaps their addressing
+    dict(B=3, H=17, T=2300, n_sub=64, d_h=32, d_v=96, W=16, R=16, bf16=True),    # 153 units: two per CTA, one idle half
+    dict(B=1, H=2, T=4100, n_sub=64, d_h=32, d_v=64, W=32, R=32, bf16=False),    # one unit per SM, uneven last window
+    dict(B=2, H=2, T=2048, n_sub=32, d_h=16, d_v=32, W=8, R=8, bf16=False, update_form=1),
+]
+
+
+@pytest.mark.parametrize("ov", SEGMENTED, ids=lambda o: "B{B}H{H}T{T}dv{d_v}".format(**o))
+def test_forward_windows_equal_address_then_scan(ov):
+    w = WORKLOADS["mid"].with_(**ov)
+    x = generate(w)
+    sh = gshape(w, sdm)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    M1, M2 = g["M0"].clone(), g["M0"].clone()
+    out = [torch.empty(w.B, w.H, w.T, n, dtype=dt, device=DEV)
+           for n, dt in ((w.W, torch.int32), (w.W, torch.float32), (w.R, torch.int32),
+                         (w.R, torch.float32))]
+    y1 = sdm.sdm_forward(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M1,
+                         None, *out)["y"]
+    sel = sdm.sdm_address(sh, g["q_w"], g["q_r"], g["K"])
+    y2 = sdm.sdm_scan(sh, *sel, g["alpha"], g["beta"], g["v"], M2)
+    torch.cuda.synchronize()
+    status_ok()
+    for a, b in zip(out, sel):
+        assert torch.equal(a, b)
+    assert torch.equal(y1, y2) and torch.equal(M1, M2)

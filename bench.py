@@ -611,7 +611,7 @@ def run_ours(args, w):
     if args.variant in ("forward", "fig2") and w.name == "gdn_matched" and w.update_form == 0:
         csrc = os.path.join(ROOT, "sparse_state_linear_gb300", "csrc")
         traffic = traffic_for([os.path.join(csrc, "plan.cu"), os.path.join(csrc, "scan.cu")])
-    launches = {"decode": 1, "logged": 3}.get(args.variant, 3)
+    launches = {"decode": 1, "logged": 3}.get(args.variant, 3 * sdm.sdm_forward_windows(sh))
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,

@@ -28,7 +28,7 @@ STATUS = {0: "SDM_OK", 1: "SDM_ERR_INVALID_ARG", 2: "SDM_ERR_UNSUPPORTED", 3: "S
 EXPORTS = ["sdm_status_string", "sdm_subscores", "sdm_select", "sdm_address",
            "sdm_workspace_size", "sdm_scan", "sdm_scan_noalloc", "sdm_scan_logged",
            "sdm_undo_workspace_size", "sdm_scan_undo", "sdm_rmsnorm_gate", "sdm_decode",
-           "sdm_forward",
+           "sdm_forward", "sdm_forward_windows",
            "sdm_get_device_status",
            "sdm_set_scan_tuning", "sdm_selftest_wait_timeout", "sdm_measure_row_traffic"]
 
@@ -100,6 +100,7 @@ def lib():
         "sdm_rmsnorm_gate": ([SP, P, P, P, ctypes.c_float, P, I, P], I),
         "sdm_decode": ([SP] + [P] * 12 + [ctypes.POINTER(Epilogue), P], I),
         "sdm_forward": ([SP] + [P] * 13 + [ctypes.c_size_t, P], I),
+        "sdm_forward_windows": ([SP], I),
         "sdm_get_device_status": ([P], I),
         "sdm_set_scan_tuning": ([I, I], I),
         "sdm_selftest_wait_timeout": ([ctypes.c_longlong, P], I),
@@ -374,6 +375,11 @@ def sdm_forward(sh: Shape, q_w, q_r, K, alpha, beta, v, M, y=None, idx_w=None, w
                           _ptr(idx_r, "idx_r", i32, n["R"]), _ptr(wt_r, "wt_r", f32, n["R"]),
                           _ptr(ws, "workspace"), nws, _stream(stream)), "sdm_forward")
     return dict(y=y, idx_w=idx_w, wt_w=wt_w, idx_r=idx_r, wt_r=wt_r)
+
+
+def sdm_forward_windows(sh: Shape) -> int:
+    """Step windows sdm_forward uses for this shape (1 = no overlap)."""
+    return int(lib().sdm_forward_windows(ctypes.byref(sh)))
 
 
 def sdm_get_device_status(stream=None) -> int:

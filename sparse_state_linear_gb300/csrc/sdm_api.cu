@@ -367,6 +367,12 @@ sdm_status sdm_scan_undo(const sdm_shape* shape, const int32_t* idx_w, const flo
                                static_cast<cudaStream_t>(stream)));
 }
 
+int sdm_forward_windows(const sdm_shape* shape) {
+  Dims d;
+  if (check_shape(shape, &d) != SDM_OK) return 0;
+  return forward_segments(d);
+}
+
 sdm_status sdm_forward(const sdm_shape* shape, const void* q_w, const void* q_r,
                        const void* K, const void* alpha, const void* beta, const void* v,
                        float* M, float* y, int32_t* idx_w, float* wt_w, int32_t* idx_r,

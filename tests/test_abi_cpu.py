@@ -208,3 +208,15 @@ def test_measure_row_traffic_arguments(L):
     # No work: nothing is launched and the pointers are not looked at.
     assert rc(None, None, 0, 1024, 128, 32, 8, 128, 64, 1, None) == 0
     assert rc(None, None, 4, 1024, 128, 32, 0, 128, 64, 1, None) == 0
+
+
+def test_forward_windows(L):
+    # Windows only from T = 2048 on; the FFMA addressing path (fp32, inverse
+    # distance, s > 256 or d_h > 64) uses 4.  (Tensor-core shapes depend on the
+    # device's shared memory and are checked in the GPU tests.)
+    assert sdm.sdm_forward_windows(good_shape(T=2047)) == 1
+    assert sdm.sdm_forward_windows(good_shape(T=8192, n_sub=512, d_h=256, d_v=512, W=8,
+                                              R=8)) == 4
+    bad = good_shape()
+    bad.W = 0
+    assert sdm.sdm_forward_windows(bad) == 0

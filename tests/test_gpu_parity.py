@@ -744,3 +744,12 @@ def test_forward_windows_equal_address_then_scan(ov):
     for a, b in zip(out, sel):
         assert torch.equal(a, b)
     assert torch.equal(y1, y2) and torch.equal(M1, M2)
+
+
+def test_forward_windows_tensor_core_shapes():
+    # Tensor-core addressing: 512-step windows, at most 32.
+    tc = dict(n_sub=256, d_h=64, d_v=128, W=64, R=64)
+    mk = lambda T: sdm.make_shape(2, 2, T, **tc)
+    assert sdm.sdm_forward_windows(mk(2047)) == 1
+    assert sdm.sdm_forward_windows(mk(4096)) == 8
+    assert sdm.sdm_forward_windows(mk(131072)) == 32

@@ -512,28 +512,39 @@ def run_ours(args, w):
             up = [torch.cuda.Event() for _ in range(n)]
             done = [torch.cuda.Event() for _ in range(n)]
             down = [torch.cuda.Event() for _ in range(n)]
-            for i in range(n + 1):
-                if i < n:
-                    with torch.cuda.stream(copy):
-                        if i >= 2:
-                            copy.wait_event(done[i - 2])     # buffer i%2 is free again
-                        for k in names:
-                            bufs[i % 2][k].copy_(host[k], non_blocking=True)
-                        up[i].record(copy)
-                if i >= 1:
-                    j = i - 1
-                    with torch.cuda.stream(copy_back):
-                        copy_back.wait_event(done[j])
-                        y_host[j % 2].copy_(y_dev[j % 2], non_blocking=True)
-                        down[j].record(copy_back)
-                if i < n:
-                    stream.wait_event(up[i])
+
+            def upload(i):
+                with torch.cuda.stream(copy):
                     if i >= 2:
-                        stream.wait_event(down[i - 2])     # y buffer i%2 was read back
+                        copy.wait_event(done[i - 2])         # buffer i%2 is free again
                     for k in names:
-                        g[k] = bufs[i % 2][k]
-                    forward_to(y_dev[i % 2])
-                    done[i].record(stream)
+                        bufs[i % 2][k].copy_(host[k], non_blocking=True)
+                    up[i].record(copy)
+
+            def read_back(j):
+                with torch.cuda.stream(copy_back):
+                    copy_back.wait_event(done[j])
+                    y_host[j % 2].copy_(y_dev[j % 2], non_blocking=True)
+                    down[j].record(copy_back)
+
+            # Step i+1's upload and step i-1's read-back are enqueued before
+            # step i's compute: a forward of many launches can fill the launch
+            # queue and block the host inside it, and the copies must not wait
+            # behind that.
+            upload(0)
+            for i in range(n):
+                if i + 1 < n:
+                    upload(i + 1)
+                if i >= 1:
+                    read_back(i - 1)
+                stream.wait_event(up[i])
+                if i >= 2:
+                    stream.wait_event(down[i - 2])         # y buffer i%2 was read back
+                for k in names:
+                    g[k] = bufs[i % 2][k]
+                forward_to(y_dev[i % 2])
+                done[i].record(stream)
+            read_back(n - 1)
             return down[n - 1]
 
         def forward_to(ydst):

@@ -48,13 +48,18 @@
 namespace sdm {
 namespace {
 
-constexpr int kConsumers = 256;
+// Consumer threads (the Fig. 2 column layout needs 8 warps: one per 16-byte
+// chunk of a 32-float slice; it only runs in the MINB = 2 build).
+template <int MINB>
+__host__ __device__ constexpr int consumer_threads() { return 256; }
 // Loader threads that fetch the rows: 4 warps where two CTAs share an SM
 // (issue slots are scarce there), 6 where a unit has the SM to itself.
 template <int MINB>
 __host__ __device__ constexpr int loader_threads() { return MINB == 1 ? 192 : 128; }
 template <int MINB>
-__host__ __device__ constexpr int scan_threads() { return kConsumers + 32 + loader_threads<MINB>(); }
+__host__ __device__ constexpr int scan_threads() {
+  return consumer_threads<MINB>() + 32 + loader_threads<MINB>();
+}
 // Producer's metadata prefetch distance (steps): the copies of a step are
 // waited for kP steps after they were issued, so at most kP steps' metadata
 // is in flight; their latency (microseconds under load) over kP bounds the
@@ -157,6 +162,9 @@ template <int CW, bool BF16, bool FIG2, bool UNDO, int MINB, int PAIR>
 __global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : MINB)
     scan_kernel(const ScanArgs A) {
   constexpr int kLoaders = loader_threads<MINB>();
+  constexpr int kConsumers = consumer_threads<MINB>();
+  constexpr int kCW = kConsumers / 32;     // consumer warps
+  static_assert(!FIG2 || kCW == 8, "the Fig. 2 layouts assume 8 consumer warps");
   constexpr int CH = CW / 4;               // 16-byte chunks per row slice
   constexpr int RP = kConsumers / CH;      // rows per consumer pass
   constexpr int IB = BF16 ? 2 : 4;         // input element bytes
@@ -589,7 +597,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : M
       const float* yp = ypart + (t & 1) * 8 * CW + 4 * lane;
       float4 s4 = *reinterpret_cast<const float4*>(yp);
 #pragma unroll
-      for (int w = 1; w < 8; ++w) {
+      for (int w = 1; w < kCW; ++w) {
         const float4 p = *reinterpret_cast<const float4*>(yp + w * CW);
         s4.x += p.x;
         s4.y += p.y;
@@ -728,7 +736,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : M
         aborted = true;
         break;
       }
-      if (t > 0 && warp == ((t - 1) & 7)) finalize(t - 1);
+      if (t > 0 && warp == ((t - 1) & (kCW - 1))) finalize(t - 1);
       // Read after the write (Eq. (5)); all of this thread's rows are read first.
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       {
@@ -781,7 +789,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : M
     }
     if (T > 0) store_partial(T - 1, acc_prev);
     named_bar_sync(bb + 1, kConsumers);
-    if (!aborted && T > 0 && warp == ((T - 1) & 7)) finalize(T - 1);
+    if (!aborted && T > 0 && warp == ((T - 1) & (kCW - 1))) finalize(T - 1);
     return;
   }
 
@@ -887,7 +895,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : M
       const float4 vv = load_v4<BF16>(m->vraw, myc);
       float4 vh = *reinterpret_cast<const float4*>(vpart + 4 * myc);
 #pragma unroll
-      for (int w = 1; w < 8; ++w) {
+      for (int w = 1; w < kCW; ++w) {
         const float4 p = *reinterpret_cast<const float4*>(vpart + w * CW + 4 * myc);
         vh.x += p.x;
         vh.y += p.y;
@@ -917,7 +925,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : M
       aborted = true;
       break;
     }
-    if (t > 0 && warp == ((t - 1) & 7)) finalize(t - 1);
+    if (t > 0 && warp == ((t - 1) & (kCW - 1))) finalize(t - 1);
 
     // Read after the write (Eq. (5)); all of this thread's rows are read first.
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -955,7 +963,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : M
   }
   if (T > 0) store_partial(T - 1, acc_prev);
   named_bar_sync(bb + 1, kConsumers);
-  if (!aborted && T > 0 && warp == ((T - 1) & 7)) finalize(T - 1);
+  if (!aborted && T > 0 && warp == ((T - 1) & (kCW - 1))) finalize(T - 1);
 }
 
 // Pair build (two units per CTA) for the Eq. (4) scan where two units share

@@ -753,3 +753,58 @@ def test_forward_windows_tensor_core_shapes():
     assert sdm.sdm_forward_windows(mk(2047)) == 1
     assert sdm.sdm_forward_windows(mk(4096)) == 8
     assert sdm.sdm_forward_windows(mk(131072)) == 32
+
+
+def test_forward_windows_in_a_captured_graph():
+    """The windowed forward forks onto the library's own streams and joins
+    back into the caller's; captured in a CUDA graph and replayed it gives
+    exactly the eager result."""
+    w = WORKLOADS["mid"].with_(B=1, H=2, T=2100)            # 4 windows
+    assert sdm.sdm_forward_windows(gshape(w, sdm)) > 1
+    x = generate(w)
+    sh = gshape(w, sdm)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    M1 = g["M0"].clone()
+    ref = sdm.sdm_forward(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M1)
+    M2 = g["M0"].clone()
+    y2 = torch.empty_like(ref["y"])
+    sel = [torch.empty_like(ref[k]) for k in ("idx_w", "wt_w", "idx_r", "wt_r")]
+    ws = torch.empty(max(16, sdm.sdm_workspace_size(sh)), dtype=torch.uint8, device=DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):                            # warm-up outside the capture
+        sdm.sdm_forward(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M2, y2,
+                        *sel, workspace=ws, stream=side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        sdm.sdm_forward(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"], M2, y2,
+                        *sel, workspace=ws, stream=side)
+    M2.copy_(g["M0"])
+    y2.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    status_ok()
+    assert torch.equal(y2, ref["y"]) and torch.equal(M2, M1)
+    for a, k in zip(sel, ("idx_w", "wt_w", "idx_r", "wt_r")):
+        assert torch.equal(a, ref[k])
+
+
+@pytest.mark.parametrize("depth,cs", [(2, 16), (5, 0)])
+def test_forward_windows_under_scan_tuning(depth, cs):
+    w = WORKLOADS["mid"].with_(B=1, H=3, T=2200)
+    x = generate(w)
+    sh = gshape(w, sdm)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    sdm.sdm_set_scan_tuning(depth, cs)
+    try:
+        M1, M2 = g["M0"].clone(), g["M0"].clone()
+        y1 = sdm.sdm_forward(sh, g["q_w"], g["q_r"], g["K"], g["alpha"], g["beta"], g["v"],
+                             M1)["y"]
+        sel = sdm.sdm_address(sh, g["q_w"], g["q_r"], g["K"])
+        y2 = sdm.sdm_scan(sh, *sel, g["alpha"], g["beta"], g["v"], M2)
+        torch.cuda.synchronize()
+        status_ok()
+        assert torch.equal(y1, y2) and torch.equal(M1, M2)
+    finally:
+        sdm.sdm_set_scan_tuning(0, 0)

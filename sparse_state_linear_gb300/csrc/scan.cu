@@ -24,8 +24,12 @@
 //
 // launch_scan runs the hazard plan (plan.cu: for every row a step touches,
 // whether its current value is the fetched copy or the on-chip copy a step
-// still in flight left, and where) and then scan_kernel, one CTA per unit:
-// 8 consumer warps, 1 producer warp and 4 loader warps.
+// still in flight left, and where) and then scan_kernel.  A unit has 8
+// consumer warps, 1 producer warp and 4 loader warps (6 where each unit has
+// an SM of its own).  Where two units share an SM, one CTA runs both units
+// side by side (separate warps, shared-memory partitions and named
+// barriers), so the launch occupies exactly units / 2 SMs and leaves the
+// rest to concurrent work; otherwise one CTA per unit.
 //  * The producer copies each step's slot lists, weights, plan codes and
 //    value slice into a ring of metadata slots (cp.async, several steps
 //    ahead) and adds the gates; it does nothing else, so its per-step work
@@ -35,11 +39,15 @@
 //    coalesced per row slice; only rows whose current value is in HBM), so
 //    depth steps of row traffic are in flight per unit; completion is an
 //    mbarrier arrive by the copies themselves.
-//  * A consumer step: test the step's rows and metadata barriers (both at
-//    once, while the previous step's read sum is reduced over the lanes),
-//    decay + delta on the write rows (kept on chip for forwarding, stored to
-//    HBM), ONE block barrier, weighted read; one warp sums the warps'
-//    partials of step t after the next barrier.
+//  * A consumer step: test the step's rows and metadata barriers (where two
+//    units share an SM, one warp tests while the others sleep in a named
+//    barrier; otherwise every warp tests, while the previous step's read sum
+//    is reduced over the lanes), decay + delta on the write rows (kept on
+//    chip for forwarding, stored to HBM), ONE block barrier, weighted read;
+//    one warp sums the warps' partials of step t after the next barrier.
+//  * Rings: write tiles 2 * depth - 1 (the oldest step a consumer may
+//    forward from to the newest a loader may be filling), read tiles depth,
+//    metadata depth + prefetch + batch + slack.
 //  Every wait is bounded (seconds); a wait that runs out records
 //  SDM_ERR_TIMEOUT in the status word and the CTA leaves cleanly.
 #include "common.cuh"

@@ -57,6 +57,20 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
                         const void* beta, const void* v, float* M, float* y, float* undo,
                         void* workspace, int depth, int col_slice, unsigned* status,
                         cudaStream_t stream);
+// The same in parts, for callers that run the plan on another stream (the
+// overlapped forward): scan_setup picks the column slice and ring depth (it
+// does not depend on T), launch_plan writes the codes for that depth, and
+// launch_scan_kernel runs the scan kernel on them.
+struct ScanSetup {
+  int cw, depth;
+  bool one_per_sm;
+};
+cudaError_t scan_setup(const Dims& d, int depth, int col_slice, bool logged, ScanSetup* out);
+cudaError_t launch_scan_kernel(const Dims& d, const ScanSetup& c, const int32_t* idx_w,
+                               const float* wt_w, const int32_t* idx_r, const float* wt_r,
+                               const void* alpha, const void* beta, const void* v, float* M,
+                               float* y, float* undo, const int16_t* codes, unsigned* status,
+                               cudaStream_t stream);
 
 // Undo of a logged segment (undo.cu): `workspace` holds B*H*N marks.
 size_t undo_workspace_bytes(const Dims& d);

@@ -1010,13 +1010,8 @@ size_t scan_workspace_bytes(const Dims& d) {
   return (size_t)d.B * d.H * d.T * code_pitch(d.W, d.R) * sizeof(int16_t);
 }
 
-cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
-                        const int32_t* idx_r, const float* wt_r, const void* alpha,
-                        const void* beta, const void* v, float* M, float* y, float* undo,
-                        void* workspace, int depth, int col_slice, unsigned* status,
-                        cudaStream_t stream) {
+cudaError_t scan_setup(const Dims& d, int depth, int col_slice, bool logged, ScanSetup* out) {
   const long long chains = (long long)d.B * d.H;
-  if (chains == 0 || d.T == 0) return cudaSuccess;
   const DeviceLimits lim = device_limits();
   const long long sms = lim.sms;
   int cw = col_slice;
@@ -1028,7 +1023,7 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   // The build that runs (see launch_t) and its metadata prefetch distance.
   const bool one = per_sm <= 1;
   const bool fig2 = d.update == SDM_UPDATE_SHARED_RESIDUAL;
-  const int kp = one && !fig2 && !undo ? prefetch_steps<1>() : prefetch_steps<2>();
+  const int kp = one && !fig2 && !logged ? prefetch_steps<1>() : prefetch_steps<2>();
   const size_t budget = per_sm <= 1    ? lim.smem_per_cta
                         : per_sm == 2 ? lim.smem_per_sm / 2 - 1024
                                       : lim.smem_per_sm / 3 - 1024;
@@ -1043,15 +1038,38 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
   if (D < 1 || D > 16) return cudaErrorInvalidValue;
   // A requested depth is a hint: shrink it until the ring fits on chip.
   while (D > 1 && scan_layout(cw, d.W, d.R, D, kp, fig2).total > lim.smem_per_cta) --D;
+  *out = ScanSetup{cw, D, one};
+  return cudaSuccess;
+}
 
-  int16_t* codes = static_cast<int16_t*>(workspace);
-  cudaError_t e = launch_plan(d, idx_w, idx_r, codes, D, status, stream);
-  if (e != cudaSuccess) return e;
-  ScanArgs A{d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, codes, M, y, undo, D, status};
+cudaError_t launch_scan_kernel(const Dims& d, const ScanSetup& c, const int32_t* idx_w,
+                               const float* wt_w, const int32_t* idx_r, const float* wt_r,
+                               const void* alpha, const void* beta, const void* v, float* M,
+                               float* y, float* undo, const int16_t* codes, unsigned* status,
+                               cudaStream_t stream) {
+  if ((long long)d.B * d.H == 0 || d.T == 0) return cudaSuccess;
+  ScanArgs A{d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, codes, M, y, undo, c.depth, status};
   const bool bf = d.in_dtype == SDM_BF16;
-  if (cw == 64) return bf ? launch_t<64, true>(A, one, stream) : launch_t<64, false>(A, one, stream);
-  if (cw == 32) return bf ? launch_t<32, true>(A, one, stream) : launch_t<32, false>(A, one, stream);
+  const bool one = c.one_per_sm;
+  if (c.cw == 64) return bf ? launch_t<64, true>(A, one, stream) : launch_t<64, false>(A, one, stream);
+  if (c.cw == 32) return bf ? launch_t<32, true>(A, one, stream) : launch_t<32, false>(A, one, stream);
   return bf ? launch_t<16, true>(A, one, stream) : launch_t<16, false>(A, one, stream);
+}
+
+cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
+                        const int32_t* idx_r, const float* wt_r, const void* alpha,
+                        const void* beta, const void* v, float* M, float* y, float* undo,
+                        void* workspace, int depth, int col_slice, unsigned* status,
+                        cudaStream_t stream) {
+  if ((long long)d.B * d.H == 0 || d.T == 0) return cudaSuccess;
+  ScanSetup c;
+  cudaError_t e = scan_setup(d, depth, col_slice, undo != nullptr, &c);
+  if (e != cudaSuccess) return e;
+  int16_t* codes = static_cast<int16_t*>(workspace);
+  e = launch_plan(d, idx_w, idx_r, codes, c.depth, status, stream);
+  if (e != cudaSuccess) return e;
+  return launch_scan_kernel(d, c, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, M, y, undo, codes,
+                            status, stream);
 }
 
 }  // namespace sdm

@@ -178,23 +178,30 @@ int run_segmented_forward(const SegmentedForward& f, int S, cudaStream_t caller)
   const int tseg = (d.T + S - 1) / S;
   const size_t qrow = (size_t)2 * d.dh * f.in_bytes;       // bytes per token of q
   const size_t CP = (size_t)code_pitch(d.W, d.R);
+  ScanSetup sc;
+  e = scan_setup(d, f.depth, f.col_slice, false, &sc);
+  // Window k's addressing on the low-priority stream; its hazard plan and
+  // scan on the high-priority one (a plan queued behind the addressing
+  // started late and held the scan back: slower on every workload).
   for (int t0 = 0; t0 < d.T && e == cudaSuccess; t0 += tseg) {
     Dims w = d;
     w.T = d.T - t0 < tseg ? d.T - t0 : tseg;
     w.Ts = d.T;
+    int32_t* iw = f.idx_w + (size_t)t0 * d.W;
+    int32_t* ir = f.idx_r + (size_t)t0 * d.R;
+    float* ww = f.wt_w + (size_t)t0 * d.W;
+    float* wr = f.wt_r + (size_t)t0 * d.R;
+    int16_t* codes = f.codes + (size_t)t0 * CP;
     e = launch_address(kAddrFused, w, f.q_w + t0 * qrow, f.q_r + t0 * qrow, f.K, nullptr,
-                       nullptr, f.idx_w + (size_t)t0 * d.W, f.wt_w + (size_t)t0 * d.W,
-                       f.idx_r + (size_t)t0 * d.R, f.wt_r + (size_t)t0 * d.R, nullptr,
-                       f.status, fs.lo);
+                       nullptr, iw, ww, ir, wr, nullptr, f.status, fs.lo);
     if (e == cudaSuccess) e = cudaEventRecord(fs.addr, fs.lo);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(fs.hi, fs.addr, 0);
+    if (e == cudaSuccess) e = launch_plan(w, iw, ir, codes, sc.depth, f.status, fs.hi);
     if (e == cudaSuccess)
-      e = launch_scan(w, f.idx_w + (size_t)t0 * d.W, f.wt_w + (size_t)t0 * d.W,
-                      f.idx_r + (size_t)t0 * d.R, f.wt_r + (size_t)t0 * d.R,
-                      f.alpha + (size_t)t0 * f.in_bytes, f.beta + (size_t)t0 * f.in_bytes,
-                      f.v + (size_t)t0 * d.dv * f.in_bytes, f.M, f.y + (size_t)t0 * d.dv,
-                      nullptr, f.codes + (size_t)t0 * CP, f.depth, f.col_slice, f.status,
-                      fs.hi);
+      e = launch_scan_kernel(w, sc, iw, ww, ir, wr, f.alpha + (size_t)t0 * f.in_bytes,
+                             f.beta + (size_t)t0 * f.in_bytes,
+                             f.v + (size_t)t0 * d.dv * f.in_bytes, f.M,
+                             f.y + (size_t)t0 * d.dv, nullptr, codes, f.status, fs.hi);
   }
   // Join both streams back into the caller's, also after a failed launch, so
   // nothing of this call is left running behind the caller's back.

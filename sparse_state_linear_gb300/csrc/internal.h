@@ -85,9 +85,10 @@ cudaError_t launch_rmsnorm_gate(const Dims& d, const float* y, const void* g, co
 // Fused decode (decode.cu): one CTA per (b,h) chain runs its T steps --
 // addressing, write, read and, when out is non-null, the epilogue.
 // sdm_api.cu: the overlapped forward (addressing of window k+1 beside the
-// scan of window k).  forward_segments gives the number of windows (1 = none);
-// run_segmented_forward returns a cudaError_t, or -1 if its streams could not
-// be set up (nothing enqueued).
+// scan of window k).  forward_window_steps gives the window length (T = no
+// windows), forward_segments the number of windows; run_segmented_forward
+// returns a cudaError_t, or -1 if its streams could not be set up (nothing
+// enqueued).
 struct SegmentedForward {
   Dims d;
   const char* q_w;
@@ -106,8 +107,9 @@ struct SegmentedForward {
   int in_bytes, depth, col_slice;
   unsigned* status;
 };
+int forward_window_steps(const Dims& d);
 int forward_segments(const Dims& d);
-int run_segmented_forward(const SegmentedForward& f, int S, cudaStream_t caller);
+int run_segmented_forward(const SegmentedForward& f, int window, cudaStream_t caller);
 
 // rowtraffic.cu: random row pieces in the scan's unit layout, no arithmetic.
 cudaError_t launch_row_traffic(const float* src, float* dst, long long chains, long long rows,

@@ -134,10 +134,20 @@ DeviceLimits device_limits() {
 // SMs it leaves free, so short windows (512 steps, at most 32 of them) hide
 // most of it; the FFMA addressing is too heavy to hide there, and only the
 // scan's per-window ramps are worth overlapping (4 windows).
+// Window length: T / windows rounded up to whole 64-step blocks (the
+// addressing CTAs take 64 tokens of a chain, the plan kernel 64 steps), so no
+// window leaves a partial block behind except the last.
+int forward_window_steps(const Dims& d) {
+  if (d.T < 2048) return d.T;
+  int s = address_on_tensor_cores(d) ? d.T / 512 : 4;
+  if (s > 32) s = 32;
+  const int len = (d.T + s - 1) / s;
+  return (len + 63) & ~63;
+}
+
 int forward_segments(const Dims& d) {
-  if (d.T < 2048) return 1;
-  const int s = address_on_tensor_cores(d) ? d.T / 512 : 4;
-  return s > 32 ? 32 : s;
+  const int len = forward_window_steps(d);
+  return len <= 0 ? 1 : (d.T + len - 1) / len;
 }
 
 namespace {
@@ -150,7 +160,7 @@ std::mutex g_fwd_mu[64];
 ForwardStreams g_fwd[64];
 }  // namespace
 
-int run_segmented_forward(const SegmentedForward& f, int S, cudaStream_t caller) {
+int run_segmented_forward(const SegmentedForward& f, int window, cudaStream_t caller) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   // Enqueueing holds the device's lock: the side streams and events are shared.
@@ -175,7 +185,7 @@ int run_segmented_forward(const SegmentedForward& f, int S, cudaStream_t caller)
   if (e == cudaSuccess) e = cudaStreamWaitEvent(fs.hi, fs.start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(fs.lo, fs.start, 0);
   if (e != cudaSuccess) return (int)e;
-  const int tseg = (d.T + S - 1) / S;
+  const int tseg = window;
   const size_t qrow = (size_t)2 * d.dh * f.in_bytes;       // bytes per token of q
   const size_t CP = (size_t)code_pitch(d.W, d.R);
   ScanSetup sc;
@@ -419,7 +429,8 @@ sdm_status sdm_forward(const sdm_shape* shape, const void* q_w, const void* q_r,
                        static_cast<const char*>(alpha), static_cast<const char*>(beta),
                        static_cast<const char*>(v), M, y, idx_w, wt_w, idx_r, wt_r,
                        static_cast<int16_t*>(workspace), ib, depth, cs, sp};
-    const int rc = run_segmented_forward(f, S, static_cast<cudaStream_t>(stream));
+    const int rc = run_segmented_forward(f, forward_window_steps(d),
+                                         static_cast<cudaStream_t>(stream));
     if (rc >= 0) return from_cuda(static_cast<cudaError_t>(rc));
     // The side streams could not be set up: one stream, unsegmented.
   }

@@ -34,9 +34,11 @@
  *    CPU fallback.
  *  - The device addresses of the library's static device arrays (the status
  *    word; the scratch of sdm_scan_noalloc) are looked up once per device and
- *    kept for the life of the process: do not go on using the library on a
- *    device after cudaDeviceReset (or any other teardown of its primary
- *    context), since those addresses are then stale.
+ *    kept for the life of the process, and so are the two streams and the
+ *    events sdm_forward uses for its overlapped windows (created on first
+ *    use): do not go on using the library on a device after cudaDeviceReset
+ *    (or any other teardown of its primary context), since those handles are
+ *    then stale.
  */
 #ifndef SDM_H
 #define SDM_H

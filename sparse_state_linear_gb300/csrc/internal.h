@@ -63,7 +63,8 @@ cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,
 // launch_scan_kernel runs the scan kernel on them.
 struct ScanSetup {
   int cw, depth;
-  bool one_per_sm;
+  bool one_per_sm;   // every unit has an SM of its own (the MINB = 1 build)
+  bool pair;         // exactly two units per SM: one CTA runs both
 };
 cudaError_t scan_setup(const Dims& d, int depth, int col_slice, bool logged, ScanSetup* out);
 cudaError_t launch_scan_kernel(const Dims& d, const ScanSetup& c, const int32_t* idx_w,

@@ -974,15 +974,14 @@ __global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : M
   if (!aborted && T > 0 && warp == ((T - 1) & (kCW - 1))) finalize(T - 1);
 }
 
-// Pair build (two units per CTA) for the Eq. (4) scan where two units share
-// an SM.
-constexpr bool kPairUnits = true;
-
 template <int CW, bool BF16>
-cudaError_t launch_t(const ScanArgs& A, bool one_per_sm, cudaStream_t stream) {
+cudaError_t launch_t(const ScanArgs& A, bool one_per_sm, bool two_per_sm, cudaStream_t stream) {
   const bool fig2 = A.d.update == SDM_UPDATE_SHARED_RESIDUAL, logged = A.undo != nullptr;
   const bool one = !fig2 && !logged && one_per_sm;      // the MINB = 1 build
-  const bool pair = kPairUnits && !fig2 && !logged && !one_per_sm;
+  // Two units per CTA for the Eq. (4) scan where exactly two units share an
+  // SM (the Fig. 2 column path measured slower that way and keeps one per
+  // CTA; with three per SM a CTA of two would not leave room for a second).
+  const bool pair = !fig2 && !logged && two_per_sm;
   const int kp = one ? prefetch_steps<1>() : prefetch_steps<2>();
   const size_t total = scan_layout(CW, A.d.W, A.d.R, A.depth, kp, fig2).total;
   const size_t smem = pair ? 2 * unit_smem_stride(total) : total;
@@ -1038,7 +1037,7 @@ cudaError_t scan_setup(const Dims& d, int depth, int col_slice, bool logged, Sca
   if (D < 1 || D > 16) return cudaErrorInvalidValue;
   // A requested depth is a hint: shrink it until the ring fits on chip.
   while (D > 1 && scan_layout(cw, d.W, d.R, D, kp, fig2).total > lim.smem_per_cta) --D;
-  *out = ScanSetup{cw, D, one};
+  *out = ScanSetup{cw, D, one, per_sm == 2};
   return cudaSuccess;
 }
 
@@ -1050,10 +1049,12 @@ cudaError_t launch_scan_kernel(const Dims& d, const ScanSetup& c, const int32_t*
   if ((long long)d.B * d.H == 0 || d.T == 0) return cudaSuccess;
   ScanArgs A{d, idx_w, wt_w, idx_r, wt_r, alpha, beta, v, codes, M, y, undo, c.depth, status};
   const bool bf = d.in_dtype == SDM_BF16;
-  const bool one = c.one_per_sm;
-  if (c.cw == 64) return bf ? launch_t<64, true>(A, one, stream) : launch_t<64, false>(A, one, stream);
-  if (c.cw == 32) return bf ? launch_t<32, true>(A, one, stream) : launch_t<32, false>(A, one, stream);
-  return bf ? launch_t<16, true>(A, one, stream) : launch_t<16, false>(A, one, stream);
+  const bool one = c.one_per_sm, two = c.pair;
+  if (c.cw == 64)
+    return bf ? launch_t<64, true>(A, one, two, stream) : launch_t<64, false>(A, one, two, stream);
+  if (c.cw == 32)
+    return bf ? launch_t<32, true>(A, one, two, stream) : launch_t<32, false>(A, one, two, stream);
+  return bf ? launch_t<16, true>(A, one, two, stream) : launch_t<16, false>(A, one, two, stream);
 }
 
 cudaError_t launch_scan(const Dims& d, const int32_t* idx_w, const float* wt_w,

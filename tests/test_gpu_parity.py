@@ -301,6 +301,24 @@ def test_scan_matches_oracle(B, H, T, s, dv, W, R, bf16, depth, cs):
             assert np.array_equal(Mg[b, h, untouched], M0[b, h, untouched])
 
 
+@pytest.mark.parametrize("B,H,dv,form", [
+    (3, 17, 96, 0),     # 153 units of 32 columns: two per CTA, one idle half (152 SMs)
+    (10, 8, 128, 0),    # 320 units: three per SM, one per CTA
+    (5, 10, 128, 1),    # Fig. 2 form at two units per SM
+])
+def test_scan_many_units_matches_oracle(B, H, dv, form):
+    """The launch configurations for more units than SMs, against the oracle
+    (small tables and T so the oracle stays quick)."""
+    T, s, W, R = 40, 16, 16, 16
+    rng = np.random.default_rng(B * 100 + H + form)
+    case = random_scan_case(rng, B, H, T, s, dv, W, R, True)
+    sh_g = sdm.make_shape(B, H, T, s, 16, dv, W, R, in_dtype=sdm.SDM_BF16, update=form)
+    Mg, yg = run_scan(sh_g, case, 0, 0)
+    Mo, yo = oracle_scan(B, H, T, s, dv, W, R, case, update_form=form)
+    assert max_rel(yg, yo) <= FTOL
+    assert max_rel(Mg, Mo) <= FTOL
+
+
 @pytest.mark.parametrize("form", [0, 1])
 @pytest.mark.parametrize("depth", [2, 4, 16])
 def test_scan_large_table_reused_rows(form, depth):

@@ -166,7 +166,9 @@ struct Ring {
 // by side (each with its own warps, shared-memory partition and named
 // barriers), so a launch of U units occupies exactly U / 2 SMs and leaves
 // the others free for concurrent work (the addressing of the next segment).
-template <int CW, bool BF16, bool FIG2, bool UNDO, int MINB, int PAIR>
+// WR: 0, or the write and read set size when both are that (64 on the
+// GDN-matched shapes), fixed at compile time so the per-row bounds fold away.
+template <int CW, bool BF16, bool FIG2, bool UNDO, int MINB, int PAIR, int WR = 0>
 __global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : MINB)
     scan_kernel(const ScanArgs A) {
   constexpr int kLoaders = loader_threads<MINB>();
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(scan_threads<MINB>() * PAIR, PAIR == 2 ? 1 : M
 
   const Dims& d = A.d;
   const int D = A.depth;
-  const int W = d.W, R = d.R, T = d.T, dv = d.dv;
+  const int W = WR ? WR : d.W, R = WR ? WR : d.R, T = d.T, dv = d.dv;
   const ScanLayout L = scan_layout(CW, W, R, D, prefetch_steps<MINB>(), FIG2);
   const int NS = L.NS, MR = L.MR;
   const int nslice = dv / CW;
@@ -982,14 +984,17 @@ cudaError_t launch_t(const ScanArgs& A, bool one_per_sm, bool two_per_sm, cudaSt
   // SM (the Fig. 2 column path measured slower that way and keeps one per
   // CTA; with three per SM a CTA of two would not leave room for a second).
   const bool pair = !fig2 && !logged && two_per_sm;
+  const bool w64 = A.d.W == 64 && A.d.R == 64;
   const int kp = one ? prefetch_steps<1>() : prefetch_steps<2>();
   const size_t total = scan_layout(CW, A.d.W, A.d.R, A.depth, kp, fig2).total;
   const size_t smem = pair ? 2 * unit_smem_stride(total) : total;
   auto kfn = fig2 ? (logged ? scan_kernel<CW, BF16, true, true, 2, 1>
                             : scan_kernel<CW, BF16, true, false, 2, 1>)
                   : (logged ? scan_kernel<CW, BF16, false, true, 2, 1>
-                            : (one ? scan_kernel<CW, BF16, false, false, 1, 1>
-                                   : (pair ? scan_kernel<CW, BF16, false, false, 2, 2>
+                            : (one ? (w64 ? scan_kernel<CW, BF16, false, false, 1, 1, 64>
+                                          : scan_kernel<CW, BF16, false, false, 1, 1>)
+                                   : (pair ? (w64 ? scan_kernel<CW, BF16, false, false, 2, 2, 64>
+                                                  : scan_kernel<CW, BF16, false, false, 2, 2>)
                                            : scan_kernel<CW, BF16, false, false, 2, 1>)));
   cudaError_t e =
       cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

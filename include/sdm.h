@@ -243,11 +243,13 @@ sdm_status sdm_decode(const sdm_shape* shape, const void* q_w, const void* q_r,
  * Inputs as above; M updated in place, y written, and the selected indices
  * and weights returned in the caller's idx_w/wt_w/idx_r/wt_r buffers. */
 /* Number of step windows sdm_forward cuts T into (1 = none; 0 for an
- * invalid shape).  With more than one, the addressing of window k+1 runs on
- * a low-priority internal stream while window k is scanned on a
- * high-priority one, both joined back into the caller's stream; results are
- * bit-identical to sdm_address followed by sdm_scan.  Each window launches
- * the addressing, plan and scan kernels once. */
+ * invalid shape): from T = 2048 on, T/512 windows (at most 32) where the
+ * addressing runs on the tensor cores, else 4; every window but the last is
+ * a whole number of 64-step blocks.  With more than one, the addressing of
+ * window k+1 runs on a low-priority internal stream while window k is
+ * scanned on a high-priority one, both joined back into the caller's
+ * stream; results are bit-identical to sdm_address followed by sdm_scan.
+ * Each window launches the addressing, plan and scan kernels once. */
 int sdm_forward_windows(const sdm_shape* shape);
 
 sdm_status sdm_forward(const sdm_shape* shape, const void* q_w, const void* q_r,

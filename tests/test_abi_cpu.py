@@ -217,6 +217,10 @@ def test_forward_windows(L):
     assert sdm.sdm_forward_windows(good_shape(T=2047)) == 1
     assert sdm.sdm_forward_windows(good_shape(T=8192, n_sub=512, d_h=256, d_v=512, W=8,
                                               R=8)) == 4
+    # Window lengths are whole 64-step blocks: T = 2100 -> 525 -> 576 steps,
+    # still 4 windows (the last one 372 steps); T = 2048 -> exactly 4 x 512.
+    for T in (2048, 2049, 2100, 4100):
+        assert sdm.sdm_forward_windows(good_shape(T=T)) == 4
     bad = good_shape()
     bad.W = 0
     assert sdm.sdm_forward_windows(bad) == 0

@@ -249,7 +249,12 @@ sdm_status sdm_decode(const sdm_shape* shape, const void* q_w, const void* q_r,
  * window k+1 runs on a low-priority internal stream while window k is
  * scanned on a high-priority one, both joined back into the caller's
  * stream; results are bit-identical to sdm_address followed by sdm_scan.
- * Each window launches the addressing, plan and scan kernels once. */
+ * Each window launches the addressing, plan and scan kernels once.  The
+ * internal streams and events are created by the first windowed call on a
+ * device: make that call outside a CUDA graph capture; later calls can be
+ * captured (the fork and join are recorded with the caller's stream).  If
+ * the streams cannot be created, sdm_forward runs unwindowed on the
+ * caller's stream. */
 int sdm_forward_windows(const sdm_shape* shape);
 
 sdm_status sdm_forward(const sdm_shape* shape, const void* q_w, const void* q_r,
